@@ -1,0 +1,177 @@
+/*
+ * tfk.h - C ABI of libtfk, the fused per-token elementwise hot path of a
+ * joint audio-video diffusion-transformer (DiT) block, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operations are the fused kernels named by the TeleFuser MiniMax H3
+ * pages: "perf(minimax-h3): add conservative DiT velocity reuse" (TeleFuser
+ * PR #38), section 2 "Lossless optimizations from PR #37", and "[FEAT] Add
+ * MiniMax H3 joint audio-video generation" (TeleFuser PR #23), "Changes
+ * Made".  The pages name the fusions but print no formula; each entry point
+ * below states the definition it computes.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *   never allocates, frees or synchronises, and keeps no state except a cache
+ *   of device attributes.  All work is enqueued on `stream` (a cudaStream_t;
+ *   NULL is the legacy default stream) and runs asynchronously.
+ * - bf16 values are passed as raw 16-bit patterns (tfk_bf16).  Arithmetic is
+ *   fp32 with fp32 accumulation; each output is rounded once to bf16, to
+ *   nearest with ties to even.
+ * - Row strides are in ELEMENTS.  bf16 row strides must be multiples of 8 and
+ *   bf16 pointers 16-byte aligned (128-bit vector access); fp32 parameter
+ *   pointers must be 16-byte aligned; int32 pointers 4-byte aligned.
+ * - Arguments are validated on the host before anything is enqueued.  On any
+ *   error the call returns a non-zero tfk_status, launches nothing and leaves
+ *   every buffer untouched; tfk_last_error_message() then describes it.
+ *   A zero-sized problem (rows == 0) is a valid no-op; its pointers may be NULL.
+ * - Launch failures return TFK_ERR_CUDA.  Faults inside a kernel surface, as
+ *   with any CUDA work, at the caller's next synchronisation.
+ * - Index inputs (mod_idx) must lie in range: that is a caller precondition,
+ *   not checked on the device (an out-of-range index reads out of bounds).
+ */
+#ifndef TFK_H
+#define TFK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TFK_OK = 0,
+    TFK_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, bad overlap, bad eps/theta */
+    TFK_ERR_MISALIGNED = 2,       /* pointer or stride breaks the alignment rules above */
+    TFK_ERR_UNSUPPORTED = 3,      /* a size outside what the kernels implement */
+    TFK_ERR_CUDA = 4              /* the CUDA runtime reported an error */
+} tfk_status;
+
+typedef uint16_t tfk_bf16; /* raw bf16 bits */
+
+#define TFK_ABI_VERSION 1
+
+/* ABI version of the loaded library (TFK_ABI_VERSION at build time). */
+int tfk_abi_version(void);
+
+/* Static English name of a status code. */
+const char* tfk_status_string(tfk_status status);
+
+/* Message describing the last non-OK status returned on the calling thread. */
+const char* tfk_last_error_message(void);
+
+/*
+ * Failure injection for host-side tests of callers' error handling: the next
+ * entry-point call on this thread that passes argument validation returns
+ * TFK_ERR_CUDA, reporting the CUDA error code `cuda_error` (> 0), instead of
+ * launching.  Nothing is sent to the GPU.  cuda_error == 0 clears a pending
+ * injection; a negative code returns TFK_ERR_INVALID_ARGUMENT.
+ */
+tfk_status tfk_debug_fail_next_launch(int32_t cuda_error);
+
+/*
+ * RMSNorm fused with indexed AdaLN modulation ("Fuse RMSNorm with indexed
+ * AdaLN modulation", TeleFuser PR #38 section 2; "indexed modulation",
+ * TeleFuser PR #23 "Changes Made").  For every row t, with m = mod_idx[t]:
+ *
+ *   inv_rms = 1 / sqrt( (1/hidden) * sum_j x[t,j]^2 + eps )
+ *   y[t,j]  = bf16( x[t,j] * inv_rms * weight[j] * (1 + scale[m,j]) + shift[m,j] )
+ *
+ * x       [rows, x_row_stride] bf16, first `hidden` columns read.
+ * y       [rows, y_row_stride] bf16, first `hidden` columns written; y == x
+ *         (same pointer and stride) runs in place; any other overlap is an error.
+ * weight  [hidden] fp32 norm weight.
+ * shift, scale  [n_mod, hidden] fp32 modulation rows (row-major, contiguous).
+ * mod_idx [rows] int32, 0 <= mod_idx[t] < n_mod (precondition).
+ * hidden  multiple of 8, 8 <= hidden <= 32768.  eps >= 0.
+ */
+tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride,
+                                     tfk_bf16* y, int64_t y_row_stride,
+                                     const float* weight, const float* shift, const float* scale,
+                                     const int32_t* mod_idx, int32_t n_mod,
+                                     int64_t rows, int32_t hidden, float eps, void* stream);
+
+/*
+ * Q/K per-head RMSNorm fused with NeoX rotate-half RoPE ("Fuse Q/K RMSNorm,
+ * RoPE, and Ulysses packing", TeleFuser PR #38 section 2; "Q/K normalization
+ * plus NeoX RoPE", TeleFuser PR #23 "Changes Made").  For q (with q_weight)
+ * and for k (with k_weight), every row t and head h, with D = head_dim:
+ *
+ *   n[d]       = v[t,h,d] / sqrt( (1/D) * sum_d v[t,h,d]^2 + eps ) * w[d]
+ *   a_i        = pos[t] * theta^(-2i/D)                          (0 <= i < D/2)
+ *   out[i]     = bf16( n[i] * cos(a_i) - n[i + D/2] * sin(a_i) )
+ *   out[i+D/2] = bf16( n[i + D/2] * cos(a_i) + n[i] * sin(a_i) )
+ *
+ * q, k          [rows, in_row_stride] bf16, each row holds n_heads heads of
+ *               head_dim values at columns [h*D, (h+1)*D); q and k may be two
+ *               column slices of one fused QKV buffer.
+ * q_out, k_out  [rows, out_row_stride] bf16, same head layout.  In place
+ *               (q_out == q and k_out == k with equal strides) is allowed.
+ * q_weight, k_weight  [head_dim] fp32, shared by every head.
+ * positions     [rows] int32 token positions (any int32 value).
+ * head_dim      multiple of 16, 16 <= head_dim <= 512; n_heads >= 1 and
+ *               2 * n_heads * G <= 2048, G = head_dim/16 rounded up to a power
+ *               of two (n_heads <= 128 at head_dim 128).
+ * theta > 0 (RoPE base, 10000 in the usual setting); eps >= 0.
+ * The angle is reduced modulo one turn exactly enough that positions up to
+ * 2^31 keep full fp32 accuracy in cos/sin.
+ */
+tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
+                                    tfk_bf16* q_out, tfk_bf16* k_out, int64_t out_row_stride,
+                                    const float* q_weight, const float* k_weight,
+                                    const int32_t* positions, int64_t rows,
+                                    int32_t n_heads, int32_t head_dim,
+                                    float theta, float eps, void* stream);
+
+/*
+ * SwiGLU on the FFN up-projection output ("SwiGLU", TeleFuser PR #23
+ * "Changes Made"):
+ *
+ *   out[t,j] = bf16( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),
+ *   g = gate_up[t, j],  u = gate_up[t, ffn + j]       (0 <= j < ffn)
+ *
+ * gate_up  [rows, in_row_stride] bf16, gate in columns [0, ffn), up in [ffn, 2*ffn).
+ * out      [rows, out_row_stride] bf16, first ffn columns written; must not
+ *          overlap gate_up.
+ * ffn      multiple of 8, >= 8.
+ */
+tfk_status tfk_swiglu(const tfk_bf16* gate_up, int64_t in_row_stride,
+                      tfk_bf16* out, int64_t out_row_stride,
+                      int64_t rows, int32_t ffn, void* stream);
+
+/*
+ * Valid-only gather ("Fuse valid-only gather with zero-tail merge", TeleFuser
+ * PR #38 section 2): copy the valid prefix of a padded token buffer into a
+ * compact buffer, bit for bit.
+ *
+ *   compact[i, :] = padded[i, :]     for 0 <= i < valid_rows
+ *
+ * padded   [>= valid_rows, hidden] bf16, contiguous rows.
+ * compact  [valid_rows, hidden] bf16, contiguous; must not overlap padded.
+ * hidden   multiple of 8.  A buffer made of several padded segments (video
+ *          then audio) is handled by one call per segment with offset pointers.
+ */
+tfk_status tfk_valid_gather(const tfk_bf16* padded, tfk_bf16* compact,
+                            int64_t valid_rows, int32_t hidden, void* stream);
+
+/*
+ * Zero-tail merge, the write-back half of the same fusion: one launch writes
+ * the compact rows back and fills the padded tail with +0.0 (bits 0x0000).
+ *
+ *   padded[i, :] = compact[i, :]     for 0 <= i < valid_rows
+ *   padded[i, :] = +0.0              for valid_rows <= i < padded_rows
+ *
+ * compact  [valid_rows, hidden] bf16, contiguous.
+ * padded   [padded_rows, hidden] bf16, contiguous; must not overlap compact.
+ * 0 <= valid_rows <= padded_rows; valid_rows == 0 zeroes the whole buffer.
+ */
+tfk_status tfk_zero_tail_merge(const tfk_bf16* compact, tfk_bf16* padded,
+                               int64_t valid_rows, int64_t padded_rows, int32_t hidden,
+                               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TFK_H */

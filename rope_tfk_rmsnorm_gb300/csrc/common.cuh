@@ -1,0 +1,139 @@
+// common.cuh - device helpers shared by the libtfk kernels (sm_103a).
+//
+// 128-bit global accesses of 8 bf16 values, bf16 <-> fp32 conversion,
+// cp.async staging into shared memory and warp reductions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tfk {
+
+// Eight bf16 values in one 16-byte vector.
+struct alignas(16) Vec8 {
+    uint32_t w[4];
+};
+
+// Streaming 16-byte load that does not allocate in L1 (each activation byte is
+// read once).  Plain (coherent) load: the in-place variants write the same
+// addresses afterwards from the same thread.
+__device__ __forceinline__ Vec8 ld_stream(const void* p) {
+    Vec8 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+// Read-only 16-byte load through the non-coherent path (inputs never written
+// by the kernel).
+__device__ __forceinline__ Vec8 ld_ro(const void* p) {
+    Vec8 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_vec(void* p, const Vec8& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+// bf16 widening is exact: the bf16 bits are the top half of the fp32 bits.
+__device__ __forceinline__ void unpack8(const Vec8& v, float f[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(v.w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(v.w[i] & 0xFFFF0000u);
+    }
+}
+
+// Two fp32 -> one bf16x2 word, round to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ Vec8 pack8(const float f[8]) {
+    Vec8 v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v.w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+// ---- cp.async staging (16 bytes per thread, bypassing L1) -----------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// Same wait with a run-time depth (a ring of `stages` buffers keeps
+// stages-1 groups in flight); the branch is uniform over the CTA.
+__device__ __forceinline__ void cp_async_wait_dyn(int pending) {
+    switch (pending) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        case 7: cp_async_wait<7>(); break;
+        case 8: cp_async_wait<8>(); break;
+        case 9: cp_async_wait<9>(); break;
+        case 10: cp_async_wait<10>(); break;
+        case 11: cp_async_wait<11>(); break;
+        case 12: cp_async_wait<12>(); break;
+        case 13: cp_async_wait<13>(); break;
+        case 14: cp_async_wait<14>(); break;
+        default: cp_async_wait<15>(); break;
+    }
+}
+
+__device__ __forceinline__ Vec8 ld_smem_vec(const void* p) {
+    Vec8 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+// ---- reductions -------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Sum over aligned groups of G lanes (G a power of two <= 32).
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+}  // namespace tfk

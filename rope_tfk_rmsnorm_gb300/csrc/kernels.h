@@ -1,0 +1,82 @@
+// kernels.h - internal launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Arguments reaching these functions have already
+// been validated by the ABI layer.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tfk {
+
+// Attributes of the current device, read once per device and cached.
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_per_block_optin;  // bytes
+    int max_smem_per_sm;           // bytes
+};
+cudaError_t device_info(DeviceInfo* out);
+
+struct AdalnArgs {
+    const uint16_t* x;
+    int64_t x_stride;
+    uint16_t* y;
+    int64_t y_stride;
+    const float* weight;
+    const float* shift;
+    const float* scale;
+    const int32_t* mod_idx;
+    int64_t rows;
+    int hidden;
+    float eps;
+};
+cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, cudaStream_t stream);
+
+struct QkRopeArgs {
+    const uint16_t* q;
+    const uint16_t* k;
+    int64_t in_stride;
+    uint16_t* q_out;
+    uint16_t* k_out;
+    int64_t out_stride;
+    const float* q_weight;
+    const float* k_weight;
+    const int32_t* pos;
+    int64_t rows;
+    int n_heads;
+    int head_dim;
+    float theta;
+    float eps;
+};
+cudaError_t launch_qk_rmsnorm_rope(const QkRopeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_swiglu(const uint16_t* gate_up, int64_t in_stride, uint16_t* out,
+                          int64_t out_stride, int64_t rows, int ffn, cudaStream_t stream);
+
+cudaError_t launch_valid_gather(const uint16_t* padded, uint16_t* compact, int64_t n_vec,
+                                cudaStream_t stream);
+
+cudaError_t launch_zero_tail_merge(const uint16_t* compact, uint16_t* padded, int64_t n_valid_vec,
+                                   int64_t n_total_vec, cudaStream_t stream);
+
+// Launch-shape choices, exposed so that the ABI layer can reject sizes the
+// kernels do not implement before anything is enqueued.
+bool rmsnorm_adaln_supported(int hidden);
+bool qk_rope_supported(int n_heads, int head_dim);
+
+}  // namespace tfk
+
+namespace tfk {
+
+// Resident CTAs per SM for `func` at this block size and dynamic shared
+// memory (raising the function's dynamic shared-memory limit when needed);
+// cached per device.  Returns 0 if the configuration cannot run.
+int blocks_per_sm(const void* func, int threads, size_t smem_bytes);
+
+// Depth of a cp.async staging ring (2..16 stages of `stage_bytes`) that keeps
+// about kInflightPerSm bytes in flight per SM when `ctas_per_sm` CTAs share
+// an SM, within the shared memory of the SM and of one CTA (`extra_bytes` of
+// other dynamic shared memory per CTA).
+constexpr int kInflightPerSm = 112 * 1024;
+int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes);
+
+}  // namespace tfk

@@ -1,0 +1,234 @@
+// rmsnorm_adaln.cu - RMSNorm fused with indexed AdaLN modulation.
+//
+// y[t,j] = bf16( x[t,j] * rsqrt(mean_j x[t,:]^2 + eps) * w[j] * (1 + scale[m,j]) + shift[m,j] ),
+// m = mod_idx[t]  ("Fuse RMSNorm with indexed AdaLN modulation", TeleFuser
+// PR #38 section 2; "indexed modulation", TeleFuser PR #23 "Changes Made").
+//
+// Design (HBM-bound: 2 bytes read + 2 bytes written per element):
+// - Persistent CTAs, each owning a contiguous run of rows, so the modulation
+//   index changes rarely inside a CTA in the packed video+audio layout.
+// - Each thread owns the same 8*V columns of every row.  The norm weight for
+//   those columns lives in registers for the whole kernel, and the shift and
+//   (1 + scale) of the current modulation row are cached in registers and
+//   re-read only when mod_idx changes (two cached rows when V == 1, so a
+//   per-token choice between two rows costs no reload).  In steady state the
+//   fp32 parameters cost no memory traffic at all.
+// - Activation rows are staged through a shared-memory ring with cp.async
+//   (16 B per thread, L1 bypassed), `stages - 1` rows ahead, so many rows are
+//   in flight per SM without holding them in registers.  A thread only reads
+//   back the slots it copied itself, so no barrier guards the ring.
+// - Sum of squares: fp32 per thread, warp shuffle, then one barrier per row
+//   through a double-buffered array of per-warp partials.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tfk {
+namespace {
+
+constexpr int kMaxThreads = 512;
+
+template <int V>
+__device__ __forceinline__ void load_mod_row(const AdalnArgs& a, int m, const int (&col)[V],
+                                             const bool (&ok)[V], float (&sh)[V][8],
+                                             float (&sc)[V][8]) {
+    const float* srow = a.shift + (int64_t)m * a.hidden;
+    const float* crow = a.scale + (int64_t)m * a.hidden;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        if (ok[i]) {
+            const float4 s0 = ld_f4(srow + col[i] * 8), s1 = ld_f4(srow + col[i] * 8 + 4);
+            const float4 c0 = ld_f4(crow + col[i] * 8), c1 = ld_f4(crow + col[i] * 8 + 4);
+            sh[i][0] = s0.x; sh[i][1] = s0.y; sh[i][2] = s0.z; sh[i][3] = s0.w;
+            sh[i][4] = s1.x; sh[i][5] = s1.y; sh[i][6] = s1.z; sh[i][7] = s1.w;
+            sc[i][0] = 1.0f + c0.x; sc[i][1] = 1.0f + c0.y; sc[i][2] = 1.0f + c0.z; sc[i][3] = 1.0f + c0.w;
+            sc[i][4] = 1.0f + c1.x; sc[i][5] = 1.0f + c1.y; sc[i][6] = 1.0f + c1.z; sc[i][7] = 1.0f + c1.w;
+        }
+    }
+}
+
+template <int V>
+__global__ void __launch_bounds__(kMaxThreads) rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Vec8* ring = reinterpret_cast<Vec8*>(smem_raw);  // [stages][nvec]
+    __shared__ float partial[2][32];
+
+    const int nvec = a.hidden >> 3;
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = (nt + 31) >> 5;
+    const float inv_hidden = 1.0f / (float)a.hidden;
+
+    const int64_t r0 = a.rows * (int64_t)blockIdx.x / gridDim.x;
+    const int64_t r1 = a.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
+    if (r0 >= r1) return;  // uniform over the CTA
+    const int nrows = (int)(r1 - r0);
+
+    int col[V];
+    bool ok[V];
+    float w[V][8];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        col[i] = tid + i * nt;
+        ok[i] = col[i] < nvec;
+        if (ok[i]) {
+            const float4 w0 = ld_f4(a.weight + col[i] * 8), w1 = ld_f4(a.weight + col[i] * 8 + 4);
+            w[i][0] = w0.x; w[i][1] = w0.y; w[i][2] = w0.z; w[i][3] = w0.w;
+            w[i][4] = w1.x; w[i][5] = w1.y; w[i][6] = w1.z; w[i][7] = w1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[i][e] = 0.f;
+        }
+    }
+
+    // Prologue: rows 0 .. stages-2 of this CTA's run go in flight.
+    for (int s = 0; s < stages - 1; ++s) {
+        if (s < nrows) {
+            const uint16_t* src = a.x + (r0 + s) * a.x_stride;
+            Vec8* dst = ring + (int64_t)s * nvec;
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (ok[i]) cp_async16(dst + col[i], src + col[i] * 8);
+        }
+        cp_async_commit();
+    }
+
+    float sh[V][8], sc[V][8];
+    float sh2[V == 1 ? V : 1][8], sc2[V == 1 ? V : 1][8];
+    int m_cur = -1, m_alt = -1;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { sh[i][e] = 0.f; sc[i][e] = 0.f; }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) { sh2[0][e] = 0.f; sc2[0][e] = 0.f; }
+    int m_next = __ldg(a.mod_idx + r0);
+
+    for (int it = 0; it < nrows; ++it) {
+        const int64_t r = r0 + it;
+        {   // keep stages-1 rows in flight
+            const int ahead = it + stages - 1;
+            if (ahead < nrows) {
+                const uint16_t* src = a.x + (r0 + ahead) * a.x_stride;
+                Vec8* dst = ring + (int64_t)(ahead % stages) * nvec;
+#pragma unroll
+                for (int i = 0; i < V; ++i)
+                    if (ok[i]) cp_async16(dst + col[i], src + col[i] * 8);
+            }
+            cp_async_commit();
+        }
+        const int m = m_next;
+        if (it + 1 < nrows) m_next = __ldg(a.mod_idx + r + 1);
+        cp_async_wait_dyn(stages - 1);
+
+        const Vec8* cur = ring + (int64_t)(it % stages) * nvec;
+        float xf[V][8];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            if (ok[i]) {
+                unpack8(ld_smem_vec(cur + col[i]), xf[i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xf[i][e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(xf[i][e], xf[i][e], ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) partial[it & 1][warp] = ss;
+        __syncthreads();
+        float total = 0.f;
+        for (int k = 0; k < nwarps; ++k) total += partial[it & 1][k];
+        const float inv_rms = rsqrtf(total * inv_hidden + a.eps);
+
+        if (m != m_cur) {  // uniform over the CTA
+            if constexpr (V == 1) {
+                if (m == m_alt) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float ts = sh[0][e], tc = sc[0][e];
+                        sh[0][e] = sh2[0][e]; sc[0][e] = sc2[0][e];
+                        sh2[0][e] = ts; sc2[0][e] = tc;
+                    }
+                    m_alt = m_cur;
+                    m_cur = m;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { sh2[0][e] = sh[0][e]; sc2[0][e] = sc[0][e]; }
+                    m_alt = m_cur;
+                    load_mod_row<V>(a, m, col, ok, sh, sc);
+                    m_cur = m;
+                }
+            } else {
+                load_mod_row<V>(a, m, col, ok, sh, sc);
+                m_cur = m;
+            }
+        }
+
+        uint16_t* dst = a.y + r * a.y_stride;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            if (ok[i]) {
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(xf[i][e] * inv_rms * w[i][e], sc[i][e], sh[i][e]);
+                st_vec(dst + col[i] * 8, pack8(o));
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
+bool choose_shape(int hidden, int* v, int* threads) {
+    const int nvec = hidden / 8;
+    for (int cand = 1; cand <= 8; cand *= 2) {
+        const int t = (nvec + cand - 1) / cand;
+        if (t <= kMaxThreads) {
+            *v = cand;
+            *threads = (t + 31) / 32 * 32;
+            return true;
+        }
+    }
+    return false;
+}
+
+template <int V>
+cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    const int row_bytes = (a.hidden / 8) * 16;
+    const void* fn = reinterpret_cast<const void*>(&rmsnorm_adaln_kernel<V>);
+    const int by_regs = blocks_per_sm(fn, threads, 0);
+    if (by_regs <= 0) return cudaErrorInvalidConfiguration;
+    const int stages = pick_stages(by_regs >= 2 ? 2 : 1, row_bytes, 0);
+    const size_t smem = (size_t)stages * row_bytes;
+    const int per_sm = blocks_per_sm(fn, threads, smem);
+    if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+    int64_t grid = (int64_t)per_sm * di.sm_count;
+    if (grid > a.rows) grid = a.rows;
+    rmsnorm_adaln_kernel<V><<<(unsigned)grid, threads, smem, stream>>>(a, stages);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool rmsnorm_adaln_supported(int hidden) {
+    int v, t;
+    return hidden > 0 && hidden % 8 == 0 && choose_shape(hidden, &v, &t);
+}
+
+cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, cudaStream_t stream) {
+    int v = 0, threads = 0;
+    if (!choose_shape(a.hidden, &v, &threads)) return cudaErrorInvalidValue;
+    switch (v) {
+        case 1: return launch_v<1>(a, threads, stream);
+        case 2: return launch_v<2>(a, threads, stream);
+        case 4: return launch_v<4>(a, threads, stream);
+        default: return launch_v<8>(a, threads, stream);
+    }
+}
+
+}  // namespace tfk

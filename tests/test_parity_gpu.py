@@ -1,0 +1,478 @@
+"""GPU parity: every entry point, called through the C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Bit-exact for gather/merge; |gpu - oracle| <= 2e-2 + 1e-2*|oracle| per
+element for the floating-point kernels.  Every output buffer is surrounded by
+canary rows (and canary padding columns where the stride is wider than the
+row), which must come back untouched.  Small and ragged cases are compared in
+full; the full-size workloads run at full size on the GPU and are compared on
+a seeded sample of rows that the oracle recomputes from freshly generated
+inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rope_tfk_rmsnorm_gb300 as tfk
+import synth
+from helpers import Guarded, THREADS, check_close, f32_dev, i32_dev, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------------------
+# runners: inputs as host arrays, outputs as host bits (+ guard checks)
+# ---------------------------------------------------------------------------
+
+def gpu_adaln(x, w, shift, scale, idx, eps, x_stride=None, y_stride=None, inplace=False):
+    rows, hidden = x.shape
+    xs = hidden if x_stride is None else x_stride
+    xbuf = Guarded(rows, hidden, xs)
+    xbuf.view.copy_(to_dev(x))
+    if inplace:
+        out = xbuf
+    else:
+        out = Guarded(rows, hidden, y_stride)
+    tfk.tfk_rmsnorm_adaln_indexed(xbuf.view, f32_dev(w), f32_dev(shift), f32_dev(scale), i32_dev(idx),
+                                  eps, out=out.view)
+    torch.cuda.synchronize()
+    out.check()
+    if not inplace:
+        xbuf.check()
+        assert np.array_equal(xbuf.host(), x), "input x was modified"
+    return out.host()
+
+
+def ora_adaln(x, w, shift, scale, idx, eps):
+    return oracle.rmsnorm_adaln_indexed(x, w, shift, scale, idx, eps, threads=THREADS)
+
+
+def gpu_qk(q, k, wq, wk, pos, H, D, theta, eps, fused=False, inplace=False, out_stride=None):
+    rows = q.shape[0]
+    width = H * D
+    if fused:  # q and k as column slices of one [rows, 3*H*D] QKV buffer
+        qkv = Guarded(rows, 3 * width)
+        qkv.view[:, :width].copy_(to_dev(q))
+        qkv.view[:, width:2 * width].copy_(to_dev(k))
+        qv, kv = qkv.view[:, :width], qkv.view[:, width:2 * width]
+    else:
+        qb, kb = Guarded(rows, width), Guarded(rows, width)
+        qb.view.copy_(to_dev(q))
+        kb.view.copy_(to_dev(k))
+        qv, kv = qb.view, kb.view
+    if inplace:
+        qo, ko = qv, kv
+    else:
+        ostride = 2 * width if fused and out_stride is None else out_stride
+        if fused:
+            ob = Guarded(rows, 2 * width, ostride)
+            qo, ko = ob.view[:, :width], ob.view[:, width:]
+        else:
+            qob, kob = Guarded(rows, width, out_stride), Guarded(rows, width, out_stride)
+            qo, ko = qob.view, kob.view
+    tfk.tfk_qk_rmsnorm_rope_neox(qv, kv, f32_dev(wq), f32_dev(wk), i32_dev(pos), H, D, theta, eps,
+                                 q_out=qo, k_out=ko)
+    torch.cuda.synchronize()
+    if fused:
+        qkv.check()
+        assert np.all(to_host(qkv.view[:, 2 * width:]) == 0xFFFF), "v columns of the QKV buffer were written"
+        if not inplace:
+            ob.check()
+    elif not inplace:
+        qob.check()
+        kob.check()
+    return to_host(qo), to_host(ko)
+
+
+def ora_qk(q, k, wq, wk, pos, H, D, theta, eps):
+    qo, ko = oracle.qk_rmsnorm_rope_neox(q, k, wq, wk, pos, H, D, theta, eps, threads=THREADS)
+    return qo.reshape(q.shape[0], H * D), ko.reshape(k.shape[0], H * D)
+
+
+def gpu_swiglu(gu, out_stride=None, in_stride=None):
+    rows, two_f = gu.shape
+    ffn = two_f // 2
+    gbuf = Guarded(rows, two_f, in_stride)
+    gbuf.view.copy_(to_dev(gu))
+    out = Guarded(rows, ffn, out_stride)
+    tfk.tfk_swiglu(gbuf.view, out=out.view)
+    torch.cuda.synchronize()
+    out.check()
+    gbuf.check()
+    return out.host()
+
+
+def ora_swiglu(gu):
+    return oracle.swiglu(gu, threads=THREADS)
+
+
+def rand_bits(rng, shape, scale=1.0):
+    v = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def mod_params(rng, n_mod, hidden, std=0.1):
+    w = (1 + 0.1 * rng.standard_normal(hidden)).astype(np.float32)
+    return (w, (std * rng.standard_normal((n_mod, hidden))).astype(np.float32),
+            (std * rng.standard_normal((n_mod, hidden))).astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm + indexed AdaLN: ragged sizes, index patterns, strides, in place
+# ---------------------------------------------------------------------------
+
+ADALN_CASES = [
+    # rows, hidden, n_mod, index pattern
+    (1, 8, 1, "const"),
+    (7, 296, 3, "random"),
+    (333, 1000, 5, "random"),
+    (300, 3072, 4, "pairs"),         # two rows alternate per token, then two others
+    (129, 5120, 2, "blocks"),
+    (1000, 4104, 6, "random"),       # 513 vectors: ragged last thread of a 2-vector layout
+    (64, 16384, 3, "random"),
+    (17, 32768, 2, "random"),        # largest hidden
+    (2500, 512, 28, "blocks"),
+]
+
+
+def index_pattern(rng, rows, n_mod, kind):
+    if kind == "const":
+        return np.zeros(rows, np.int32)
+    if kind == "random":
+        return rng.integers(0, n_mod, rows).astype(np.int32)
+    if kind == "pairs":
+        half = rows // 2
+        return np.r_[rng.integers(0, 2, half), 2 + rng.integers(0, 2, rows - half)].astype(np.int32) % n_mod
+    return (np.arange(rows) * n_mod // rows).astype(np.int32)
+
+
+@pytest.mark.parametrize("rows,hidden,n_mod,kind", ADALN_CASES)
+def test_adaln_ragged(cuda, rows, hidden, n_mod, kind):
+    rng = np.random.default_rng(rows * 7 + hidden)
+    x = rand_bits(rng, (rows, hidden), 2.0)
+    w, sh, sc = mod_params(rng, n_mod, hidden)
+    idx = index_pattern(rng, rows, n_mod, kind)
+    got = gpu_adaln(x, w, sh, sc, idx, 1e-6)
+    check_close(got, ora_adaln(x, w, sh, sc, idx, 1e-6), f"adaln {rows}x{hidden}")
+
+
+def test_adaln_strided_and_in_place(cuda):
+    rng = np.random.default_rng(1)
+    rows, hidden = 211, 3072
+    x = rand_bits(rng, (rows, hidden))
+    w, sh, sc = mod_params(rng, 3, hidden)
+    idx = rng.integers(0, 3, rows).astype(np.int32)
+    ref = ora_adaln(x, w, sh, sc, idx, 1e-6)
+    check_close(gpu_adaln(x, w, sh, sc, idx, 1e-6, x_stride=hidden + 64, y_stride=hidden + 8), ref, "strided")
+    check_close(gpu_adaln(x, w, sh, sc, idx, 1e-6, x_stride=hidden + 64, inplace=True), ref, "in place")
+
+
+def test_adaln_degenerate_rows(cuda):
+    # zero rows give shift exactly; a constant row gives c/sqrt(c^2+eps) modulated
+    hidden = 512
+    x = np.zeros((4, hidden), np.uint16)
+    x[1] = 0x3F80  # 1.0
+    x[2] = 0x3A83  # ~1e-3: eps matters
+    x[3] = 0xC2C8  # -100
+    rng = np.random.default_rng(3)
+    w, sh, sc = mod_params(rng, 2, hidden)
+    idx = np.array([0, 1, 0, 1], np.int32)
+    got = gpu_adaln(x, w, sh, sc, idx, 1e-6)
+    ref = ora_adaln(x, w, sh, sc, idx, 1e-6)
+    check_close(got, ref, "degenerate rows")
+    assert np.array_equal(got[0], oracle.round_bf16(sh[0].astype(np.float64)))
+
+
+def test_adaln_empty_is_a_no_op(cuda):
+    out = Guarded(0, 512)
+    x = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros(512, dtype=torch.float32, device="cuda")
+    tfk.tfk_rmsnorm_adaln_indexed(x, z, z[None], z[None], torch.empty(0, dtype=torch.int32, device="cuda"),
+                                  out=out.view)
+    torch.cuda.synchronize()
+    out.check()
+
+
+def test_adaln_bad_arguments_raise_and_write_nothing(cuda):
+    out = Guarded(8, 12)
+    x = torch.zeros((8, 12), dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros(12, dtype=torch.float32, device="cuda")
+    with pytest.raises(tfk.TfkError) as e:
+        tfk.tfk_rmsnorm_adaln_indexed(x, z, z[None], z[None], torch.zeros(8, dtype=torch.int32, device="cuda"),
+                                      out=out.view)
+    assert e.value.status == 3  # hidden 12 is not a multiple of 8
+    torch.cuda.synchronize()
+    out.check()
+    assert np.all(out.host() == 0xFFFF)
+
+
+# ---------------------------------------------------------------------------
+# Q/K RMSNorm + NeoX RoPE
+# ---------------------------------------------------------------------------
+
+QK_CASES = [
+    # rows, heads, head_dim
+    (5, 1, 16),
+    (33, 3, 64),
+    (65, 5, 96),       # 6 lanes per head in a group of 8
+    (300, 24, 128),
+    (77, 40, 128),
+    (19, 128, 128),    # most heads at head_dim 128 (4 head slots per thread)
+    (11, 4, 256),
+    (9, 2, 512),
+]
+
+
+@pytest.mark.parametrize("rows,H,D", QK_CASES)
+def test_qk_ragged(cuda, rows, H, D):
+    rng = np.random.default_rng(rows + H * D)
+    q = rand_bits(rng, (rows, H * D), 3.0)
+    k = rand_bits(rng, (rows, H * D), 0.5)
+    wq = (1 + 0.2 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.2 * rng.standard_normal(D)).astype(np.float32)
+    pos = rng.integers(0, 80000, rows).astype(np.int32)
+    qo, ko = gpu_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6)
+    rq, rk = ora_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6)
+    check_close(qo, rq, f"q {rows}x{H}x{D}")
+    check_close(ko, rk, f"k {rows}x{H}x{D}")
+
+
+def test_qk_fused_qkv_layout_in_place_and_out_of_place(cuda):
+    rng = np.random.default_rng(5)
+    rows, H, D = 97, 8, 128
+    q = rand_bits(rng, (rows, H * D))
+    k = rand_bits(rng, (rows, H * D))
+    wq = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    pos = np.arange(rows, dtype=np.int32) * 613
+    rq, rk = ora_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6)
+    for inplace in (False, True):
+        qo, ko = gpu_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6, fused=True, inplace=inplace)
+        check_close(qo, rq, f"fused q inplace={inplace}")
+        check_close(ko, rk, f"fused k inplace={inplace}")
+    qo, ko = gpu_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6, out_stride=H * D + 24)
+    check_close(qo, rq, "padded-stride q")
+
+
+def test_qk_extreme_positions_and_bases(cuda):
+    # negative positions and positions near 2^31 - 1: the angle reduction is exact mod one turn
+    rng = np.random.default_rng(8)
+    rows, H, D = 64, 2, 128
+    q = rand_bits(rng, (rows, H * D))
+    k = rand_bits(rng, (rows, H * D))
+    w = np.ones(D, np.float32)
+    pos = np.r_[rng.integers(-2**31, 2**31 - 1, rows - 4), [0, -1, 2**31 - 1, -2**31]].astype(np.int32)
+    for theta in (10000.0, 500000.0, 10.0):
+        qo, ko = gpu_qk(q, k, w, w, pos, H, D, theta, 1e-6)
+        rq, rk = ora_qk(q, k, w, w, pos, H, D, theta, 1e-6)
+        check_close(qo, rq, f"q theta={theta}")
+        check_close(ko, rk, f"k theta={theta}")
+
+
+def test_qk_position_zero_is_plain_head_rmsnorm(cuda):
+    rng = np.random.default_rng(9)
+    rows, H, D = 40, 6, 64
+    q = rand_bits(rng, (rows, H * D))
+    w = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    qo, _ = gpu_qk(q, q, w, w, np.zeros(rows, np.int32), H, D, 10000.0, 1e-6)
+    ref = oracle.head_rmsnorm(q, H, D, w, 1e-6).reshape(rows, H * D)
+    check_close(qo, ref, "pos 0")
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,ffn", [(1, 8), (5, 104), (300, 1024), (37, 13824), (3, 8200)])
+def test_swiglu_ragged(cuda, rows, ffn):
+    rng = np.random.default_rng(rows * 31 + ffn)
+    gu = rand_bits(rng, (rows, 2 * ffn), 4.0)
+    check_close(gpu_swiglu(gu), ora_swiglu(gu), f"swiglu {rows}x{ffn}")
+
+
+def test_swiglu_strides_and_extremes(cuda):
+    rng = np.random.default_rng(2)
+    rows, ffn = 64, 512
+    g = rng.standard_normal((rows, ffn)) * 3
+    g[0, :8] = [0.0, -0.0, 1.0, -1.0, 90.0, -90.0, 300.0, -300.0]
+    u = rng.standard_normal((rows, ffn))
+    gu = torch.from_numpy(np.concatenate([g, u], 1).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    check_close(gpu_swiglu(gu, out_stride=ffn + 8, in_stride=2 * ffn + 16), ora_swiglu(gu), "swiglu strided")
+
+
+# ---------------------------------------------------------------------------
+# valid-only gather / zero-tail merge (bit-exact)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,L,hidden", [(1, 0, 8), (1, 1, 8), (100, 37, 24), (4096, 4095, 3072),
+                                        (1000, 1000, 512), (513, 0, 64)])
+def test_gather_merge_bit_exact(cuda, N, L, hidden):
+    rng = np.random.default_rng(N + L)
+    padded = rng.integers(0, 65536, (N, hidden), dtype=np.uint32).astype(np.uint16)
+    padded[L:] = synth.BF16_NAN
+    dev = to_dev(padded)
+    comp = Guarded(L, hidden)
+    tfk.tfk_valid_gather(dev, L, compact=comp.view)
+    torch.cuda.synchronize()
+    comp.check()
+    assert np.array_equal(comp.host(), oracle.valid_gather(padded, L))
+    back = Guarded(N, hidden)
+    tfk.tfk_zero_tail_merge(comp.view, back.view)
+    torch.cuda.synchronize()
+    back.check()
+    merged = back.host()
+    assert np.array_equal(merged, oracle.zero_tail_merge(oracle.valid_gather(padded, L), N))
+    assert np.all(merged[L:] == 0x0000)
+
+
+# ---------------------------------------------------------------------------
+# the workloads
+# ---------------------------------------------------------------------------
+
+def _inputs_dev(wl, tags, rows=None):
+    host = {t: synth.activation(wl, t, rows=rows) for t in tags}
+    return host, {t: to_dev(a) for t, a in host.items()}
+
+
+def _params_dev(wl):
+    p = synth.params(wl)
+    return p, {k: f32_dev(v) for k, v in p.items()}
+
+
+def _chain_full(wl):
+    """Whole-workload chain on the GPU, full oracle comparison (small workloads)."""
+    host, dev = _inputs_dev(wl, ["x", "q", "k", "gate_up"])
+    p, pd = _params_dev(wl)
+    idx, pos = synth.mod_index(wl), synth.positions(wl)
+    y = tfk.tfk_rmsnorm_adaln_indexed(dev["x"], pd["w"], pd["shift"], pd["scale"], i32_dev(idx), wl.eps)
+    qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(dev["q"], dev["k"], pd["w_q"], pd["w_k"], i32_dev(pos),
+                                          wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    o = tfk.tfk_swiglu(dev["gate_up"])
+    torch.cuda.synchronize()
+    stats = {"a1": check_close(to_host(y), ora_adaln(host["x"], p["w"], p["shift"], p["scale"], idx, wl.eps),
+                               f"{wl.name} a1")}
+    rq, rk = ora_qk(host["q"], host["k"], p["w_q"], p["w_k"], pos, wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    stats["a2q"] = check_close(to_host(qo), rq, f"{wl.name} a2 q")
+    stats["a2k"] = check_close(to_host(ko), rk, f"{wl.name} a2 k")
+    stats["a3"] = check_close(to_host(o), ora_swiglu(host["gate_up"]), f"{wl.name} a3")
+    return stats
+
+
+def test_tiny_chain(cuda):
+    stats = _chain_full(synth.get("tiny"))
+    assert all(s["bit_equal"] > 0.9 for s in stats.values()), stats
+
+
+def test_medium_chain(cuda):
+    _chain_full(synth.get("medium"))
+
+
+def test_valid_only_pipeline(cuda):
+    """gather X, Q, K -> a1 and a2 on the valid rows only -> merge back: the tail is exactly +0.0."""
+    wl = synth.get("valid_only")
+    N, L, hidden = wl.rows, synth.valid_len(wl), wl.hidden
+    host, dev = _inputs_dev(wl, ["x", "q", "k"])
+    p, pd = _params_dev(wl)
+    idx = synth.mod_index(wl, np.arange(L))
+    pos = synth.positions(wl, np.arange(L))
+    compact = {}
+    for t in ("x", "q", "k"):
+        compact[t] = tfk.tfk_valid_gather(dev[t], L)
+    torch.cuda.synchronize()
+    for t in ("x", "q", "k"):
+        assert np.array_equal(to_host(compact[t]), oracle.valid_gather(host[t], L)), f"gather {t}"
+    y = tfk.tfk_rmsnorm_adaln_indexed(compact["x"], pd["w"], pd["shift"], pd["scale"], i32_dev(idx), wl.eps)
+    qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(compact["q"], compact["k"], pd["w_q"], pd["w_k"], i32_dev(pos),
+                                          wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    outs = {}
+    for t, c in (("y", y), ("q", qo), ("k", ko)):
+        g = Guarded(N, hidden)  # pre-filled with 0xFFFF: every row must be rewritten
+        tfk.tfk_zero_tail_merge(c, g.view)
+        outs[t] = (c, g)
+    torch.cuda.synchronize()
+    xc = oracle.valid_gather(host["x"], L)
+    check_close(to_host(y), ora_adaln(xc, p["w"], p["shift"], p["scale"], idx, wl.eps), "valid-only a1")
+    rq, rk = ora_qk(oracle.valid_gather(host["q"], L), oracle.valid_gather(host["k"], L), p["w_q"], p["w_k"],
+                    pos, wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    check_close(to_host(qo), rq, "valid-only a2 q")
+    check_close(to_host(ko), rk, "valid-only a2 k")
+    for t, (c, g) in outs.items():
+        g.check()
+        merged = g.host()
+        assert np.array_equal(merged, oracle.zero_tail_merge(to_host(c), N)), f"merge {t}"
+        assert np.all(merged[L:] == 0x0000) and not np.any(np.isnan(oracle.bf16_to_f64(merged)))
+
+
+def _sampled_chain(wl, n_sample=192):
+    """Full-size chain on the GPU; the oracle recomputes a seeded sample of rows."""
+    rows = synth.sample_rows(wl, n_sample)
+    p, pd = _params_dev(wl)
+    idx_all, pos_all = synth.mod_index(wl), synth.positions(wl)
+    stats = {}
+    # one step at a time to bound device memory: inputs of a step are freed before the next
+    _, dev = _inputs_dev(wl, ["x"])
+    y = tfk.tfk_rmsnorm_adaln_indexed(dev["x"], pd["w"], pd["shift"], pd["scale"], i32_dev(idx_all), wl.eps)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y.float()).all())
+    ys = to_host(y[torch.from_numpy(rows).cuda()])
+    del dev, y
+    xs = synth.activation(wl, "x", rows=rows)
+    stats["a1"] = check_close(ys, ora_adaln(xs, p["w"], p["shift"], p["scale"], idx_all[rows], wl.eps),
+                              f"{wl.name} a1")
+    _, dev = _inputs_dev(wl, ["q", "k"])
+    qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(dev["q"], dev["k"], pd["w_q"], pd["w_k"], i32_dev(pos_all),
+                                          wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    torch.cuda.synchronize()
+    sel = torch.from_numpy(rows).cuda()
+    qs, ks = to_host(qo[sel]), to_host(ko[sel])
+    del dev, qo, ko
+    rq, rk = ora_qk(synth.activation(wl, "q", rows=rows), synth.activation(wl, "k", rows=rows),
+                    p["w_q"], p["w_k"], pos_all[rows], wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    stats["a2q"] = check_close(qs, rq, f"{wl.name} a2 q")
+    stats["a2k"] = check_close(ks, rk, f"{wl.name} a2 k")
+    _, dev = _inputs_dev(wl, ["gate_up"])
+    o = tfk.tfk_swiglu(dev["gate_up"])
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(o.float()).all())
+    os_ = to_host(o[torch.from_numpy(rows).cuda()])
+    del dev, o
+    stats["a3"] = check_close(os_, ora_swiglu(synth.activation(wl, "gate_up", rows=rows)), f"{wl.name} a3")
+    torch.cuda.empty_cache()
+    return stats
+
+
+def test_large_sampled(cuda):
+    _sampled_chain(synth.get("large"))
+
+
+def test_per_frame_sampled(cuda):
+    _sampled_chain(synth.get("per_frame"))
+
+
+def test_over_2g_elements_indexing(cuda):
+    """SwiGLU and the merge on buffers of more than 2^31 elements (64-bit indexing):
+    a seeded block is tiled on the device and sampled rows are checked."""
+    rng = np.random.default_rng(11)
+    ffn, rows = 14336, 75000                           # gate_up: 75000 x 28672 = 2.15e9 elements
+    block = rand_bits(rng, (64, 2 * ffn), 3.0)
+    gu = to_dev(block).repeat(rows // 64 + 1, 1)[:rows]
+    assert gu.numel() > 2**31
+    o = tfk.tfk_swiglu(gu)
+    torch.cuda.synchronize()
+    sample = np.r_[0, 1, rng.integers(0, rows, 60), rows - 1]
+    check_close(to_host(o[torch.from_numpy(sample).cuda()]), ora_swiglu(block[sample % 64]), "swiglu > 2^31")
+    del o
+    hidden, N = 8192, 270000                           # 2.2e9 elements
+    L = N - 12345
+    comp = to_dev(block[:, :hidden]).repeat(L // 64 + 1, 1)[:L]
+    padded = torch.empty((N, hidden), dtype=torch.bfloat16, device="cuda")
+    tfk.tfk_zero_tail_merge(comp, padded)
+    torch.cuda.synchronize()
+    tail = padded[L:].view(torch.int16)
+    assert int((tail != 0).sum()) == 0
+    idx = torch.from_numpy(np.r_[0, L - 1, rng.integers(0, L, 30)]).cuda()
+    assert torch.equal(padded[idx].view(torch.int16), comp[idx].view(torch.int16))
+    del gu, comp, padded
+    torch.cuda.empty_cache()
