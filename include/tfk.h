@@ -170,6 +170,28 @@ tfk_status tfk_zero_tail_merge(const tfk_bf16* compact, tfk_bf16* padded,
                                int64_t valid_rows, int64_t padded_rows, int32_t hidden,
                                void* stream);
 
+/*
+ * Conservative DiT velocity-cache schedule ("perf(minimax-h3): add
+ * conservative DiT velocity reuse", TeleFuser PR #38, section 3).  Host-only:
+ * no GPU work, no stream.
+ *
+ * reuse[i] = 1 when step i (0-based, progress i/num_steps) may skip the DiT
+ * call and reuse the previous video/audio velocity: the progress lies in
+ * [start_ratio, end_ratio), a velocity was computed on an earlier step, and
+ * fewer than min(max_consecutive_reuse, refresh_interval - 1) steps in a row
+ * have reused it since the last DiT call.  reuse[i] = 0 means the DiT runs.
+ * The page's defaults are 0.2, 0.8, 2, 1; over 49 steps they give 15 hits
+ * and 34 DiT calls.
+ *
+ * reuse      [num_steps] HOST array written by the call (may be NULL if num_steps == 0).
+ * num_reuse  optional HOST pointer receiving the number of hits.
+ * Errors: TFK_ERR_INVALID_ARGUMENT for num_steps < 0, refresh_interval < 1,
+ * max_consecutive_reuse < 0, ratios outside 0 <= start <= end <= 1, or a NULL reuse.
+ */
+tfk_status tfk_velocity_cache_schedule(int32_t num_steps, double start_ratio, double end_ratio,
+                                       int32_t refresh_interval, int32_t max_consecutive_reuse,
+                                       uint8_t* reuse, int32_t* num_reuse);
+
 #ifdef __cplusplus
 }
 #endif

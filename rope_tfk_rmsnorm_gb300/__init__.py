@@ -36,6 +36,8 @@ SIGNATURES = [
     ("tfk_swiglu", ctypes.c_int, [_vp, _i64, _vp, _i64, _i64, _i32, _vp]),
     ("tfk_valid_gather", ctypes.c_int, [_vp, _vp, _i64, _i32, _vp]),
     ("tfk_zero_tail_merge", ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp]),
+    ("tfk_velocity_cache_schedule", ctypes.c_int,
+     [_i32, ctypes.c_double, ctypes.c_double, _i32, _i32, _vp, _vp]),
 ]
 
 _lock = threading.Lock()
@@ -186,3 +188,16 @@ def tfk_zero_tail_merge(compact: torch.Tensor, padded: torch.Tensor, valid_rows:
     _check(load().tfk_zero_tail_merge(_ptr(compact), _ptr(padded), L, padded.shape[0], padded.shape[1],
                                       _stream(padded, stream)))
     return padded
+
+
+def tfk_velocity_cache_schedule(num_steps: int, start_ratio: float = 0.2, end_ratio: float = 0.8,
+                                refresh_interval: int = 2, max_consecutive_reuse: int = 1) -> list:
+    """Per step: True where the conservative velocity cache reuses the previous velocity."""
+    buf = (ctypes.c_uint8 * max(1, num_steps))()
+    hits = ctypes.c_int32(0)
+    st = load().tfk_velocity_cache_schedule(num_steps, start_ratio, end_ratio, refresh_interval,
+                                            max_consecutive_reuse, ctypes.cast(buf, ctypes.c_void_p),
+                                            ctypes.cast(ctypes.pointer(hits), ctypes.c_void_p))
+    if st != TFK_OK:
+        raise TfkError(st, "tfk_velocity_cache_schedule: invalid arguments")
+    return [bool(buf[i]) for i in range(num_steps)]

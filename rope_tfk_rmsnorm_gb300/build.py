@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtfk.so")
 
-SOURCES = ["api.cu", "rmsnorm_adaln.cu", "qk_rmsnorm_rope.cu", "swiglu.cu", "gather_merge.cu"]
+SOURCES = ["api.cu", "rmsnorm_adaln.cu", "qk_rmsnorm_rope.cu", "swiglu.cu", "gather_merge.cu",
+           "velocity_cache.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 
@@ -53,7 +54,7 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) 
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
 
     def compile_one(src: str):
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
