@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tfk", "reference"], default="tfk")
     ap.add_argument("--workload", default="large", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--rows", type=int, default=0,
+                    help="use only the first ROWS tokens of the workload (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="time box of the oracle baseline")
     ap.add_argument("--no-valid-only", action="store_true")
@@ -420,6 +422,16 @@ def run_reference(args, ranks: Ranks) -> dict | None:
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def prefix(wl, rows: int):
+    """The first `rows` tokens of a workload (video rows first), same recipe; 0 = all."""
+    import dataclasses
+    if rows <= 0 or rows >= wl.rows:
+        return wl
+    n_video = min(wl.n_video, rows)
+    return dataclasses.replace(wl, rows=rows, n_video=n_video, n_audio=rows - n_video,
+                               n_outliers=wl.n_outliers * rows // wl.rows)
+
+
 def workload_config(wl) -> dict:
     return {"workload": f"{wl.name}: {wl.rows} tokens ({wl.n_video} video + {wl.n_audio} audio), hidden "
                         f"{wl.hidden}, {wl.n_heads}x{wl.head_dim} heads, ffn {wl.ffn}, {wl.n_mod} modulation rows",
@@ -479,7 +491,7 @@ def run_tfk(args, ranks: Ranks) -> dict | None:
         raise RuntimeError("bench.py needs a CUDA GPU")
     device = torch.device("cuda", ranks.local_rank)
     torch.cuda.set_device(device)
-    wl = synth.get(args.workload)
+    wl = prefix(synth.get(args.workload), args.rows)
     if ranks.world > 1:  # weak scaling: each rank its own batch of the same shape
         wl = dataclasses.replace(wl, seed=wl.seed + ranks.rank)
     peaks = measured_peaks()

@@ -125,6 +125,38 @@ tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_
                                     float theta, float eps, void* stream);
 
 /*
+ * Fixed-valid mode of the two normalisation kernels ("Add fixed-valid and
+ * valid-only attention modes" and "Fuse valid-only gather with zero-tail
+ * merge", TeleFuser PR #38 section 2): the kernel works directly on the padded
+ * token buffer.  Rows [0, valid_rows) are computed exactly as by the entry
+ * points above (reading only those rows of the inputs, mod_idx and
+ * positions); rows [valid_rows, padded_rows) of the outputs are written +0.0
+ * (0x0000) in the same launch and the padded tail of the inputs is never
+ * read.  With this mode the valid-only pipeline needs no gather and no merge.
+ *
+ * Arguments as for the entry points above, with rows replaced by
+ * 0 <= valid_rows <= padded_rows; outputs hold padded_rows rows; inputs need
+ * only valid_rows rows.  Outputs may be the inputs (same pointer and stride);
+ * any other overlap with the padded output region is an error.
+ */
+tfk_status tfk_rmsnorm_adaln_indexed_fixed_valid(const tfk_bf16* x, int64_t x_row_stride,
+                                                 tfk_bf16* y, int64_t y_row_stride,
+                                                 const float* weight, const float* shift,
+                                                 const float* scale, const int32_t* mod_idx,
+                                                 int32_t n_mod, int64_t valid_rows,
+                                                 int64_t padded_rows, int32_t hidden, float eps,
+                                                 void* stream);
+
+tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf16* k,
+                                                int64_t in_row_stride, tfk_bf16* q_out,
+                                                tfk_bf16* k_out, int64_t out_row_stride,
+                                                const float* q_weight, const float* k_weight,
+                                                const int32_t* positions, int64_t valid_rows,
+                                                int64_t padded_rows, int32_t n_heads,
+                                                int32_t head_dim, float theta, float eps,
+                                                void* stream);
+
+/*
  * SwiGLU on the FFN up-projection output ("SwiGLU", TeleFuser PR #23
  * "Changes Made"):
  *

@@ -236,3 +236,25 @@ def zero_tail_merge(compact: np.ndarray, padded_rows: int) -> np.ndarray:
     if padded_rows and hidden:
         _load().oracle_zero_tail_merge(_p(compact), valid_rows, padded_rows, hidden, _p(out))
     return out
+
+
+# ---- fixed-valid mode: the same definitions on the valid prefix, +0.0 after it ----
+
+def rmsnorm_adaln_fixed_valid(x_padded: np.ndarray, valid_rows: int, weight, shift, scale, mod_idx, eps,
+                              threads: int = 1) -> np.ndarray:
+    """rmsnorm_adaln_indexed on rows [0, valid_rows); +0.0 on the rest of the padded rows."""
+    out = np.zeros((x_padded.shape[0], x_padded.shape[1]), dtype=np.float64)
+    out[:valid_rows] = rmsnorm_adaln_indexed(x_padded[:valid_rows], weight, shift, scale,
+                                             np.asarray(mod_idx)[:valid_rows], eps, threads=threads)
+    return out
+
+
+def qk_rmsnorm_rope_neox_fixed_valid(q_padded, k_padded, valid_rows: int, q_weight, k_weight, pos,
+                                     n_heads: int, head_dim: int, base: float, eps: float, threads: int = 1):
+    """qk_rmsnorm_rope_neox on rows [0, valid_rows); +0.0 on the rest of the padded rows."""
+    shape = (q_padded.shape[0], n_heads, head_dim)
+    qo, ko = np.zeros(shape), np.zeros(shape)
+    qo[:valid_rows], ko[:valid_rows] = qk_rmsnorm_rope_neox(q_padded[:valid_rows], k_padded[:valid_rows],
+                                                            q_weight, k_weight, np.asarray(pos)[:valid_rows],
+                                                            n_heads, head_dim, base, eps, threads=threads)
+    return qo, ko

@@ -33,6 +33,10 @@ SIGNATURES = [
      [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _f32, _vp]),
     ("tfk_qk_rmsnorm_rope_neox", ctypes.c_int,
      [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp]),
+    ("tfk_rmsnorm_adaln_indexed_fixed_valid", ctypes.c_int,
+     [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _f32, _vp]),
+    ("tfk_qk_rmsnorm_rope_neox_fixed_valid", ctypes.c_int,
+     [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _f32, _f32, _vp]),
     ("tfk_swiglu", ctypes.c_int, [_vp, _i64, _vp, _i64, _i64, _i32, _vp]),
     ("tfk_valid_gather", ctypes.c_int, [_vp, _vp, _i64, _i32, _vp]),
     ("tfk_zero_tail_merge", ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp]),
@@ -145,6 +149,54 @@ def tfk_qk_rmsnorm_rope_neox(q: torch.Tensor, k: torch.Tensor, q_weight: torch.T
     _check(load().tfk_qk_rmsnorm_rope_neox(_ptr(q), _ptr(k), qs, _ptr(q_out), _ptr(k_out), qos,
                                            _ptr(q_weight), _ptr(k_weight), _ptr(positions), rows,
                                            n_heads, head_dim, theta, eps, _stream(q, stream)))
+    return q_out, k_out
+
+
+def tfk_rmsnorm_adaln_indexed_fixed_valid(x: torch.Tensor, valid_rows: int, weight: torch.Tensor,
+                                          shift: torch.Tensor, scale: torch.Tensor, mod_idx: torch.Tensor,
+                                          eps: float = 1e-6, out: torch.Tensor | None = None,
+                                          stream=None) -> torch.Tensor:
+    """Fixed-valid RMSNorm+AdaLN on a padded buffer x [padded_rows, hidden]: rows < valid_rows
+    as tfk_rmsnorm_adaln_indexed, the rest of out written +0.0; mod_idx holds valid_rows entries."""
+    xs = _rows(x, "x")
+    padded, hidden = x.shape
+    for t, n in ((weight, "weight"), (shift, "shift"), (scale, "scale")):
+        _param(t, n)
+    _param(mod_idx, "mod_idx", torch.int32)
+    if out is None:
+        out = torch.empty((padded, hidden), dtype=torch.bfloat16, device=x.device)
+    ys = _rows(out, "out")
+    _check(load().tfk_rmsnorm_adaln_indexed_fixed_valid(
+        _ptr(x), xs, _ptr(out), ys, _ptr(weight), _ptr(shift), _ptr(scale), _ptr(mod_idx),
+        shift.shape[0] if shift.dim() == 2 else 1, valid_rows, out.shape[0], hidden, eps, _stream(x, stream)))
+    return out
+
+
+def tfk_qk_rmsnorm_rope_neox_fixed_valid(q: torch.Tensor, k: torch.Tensor, valid_rows: int,
+                                         q_weight: torch.Tensor, k_weight: torch.Tensor,
+                                         positions: torch.Tensor, n_heads: int, head_dim: int,
+                                         theta: float = 10000.0, eps: float = 1e-6,
+                                         q_out: torch.Tensor | None = None, k_out: torch.Tensor | None = None,
+                                         stream=None):
+    """Fixed-valid Q/K RMSNorm+RoPE on padded q, k [padded_rows, >= n_heads*head_dim]."""
+    qs, ks = _rows(q, "q"), _rows(k, "k")
+    if qs != ks or q.shape[0] != k.shape[0]:
+        raise ValueError("q and k must have the same rows and row stride")
+    padded = q.shape[0]
+    width = n_heads * head_dim
+    _param(q_weight, "q_weight")
+    _param(k_weight, "k_weight")
+    _param(positions, "positions", torch.int32)
+    if q_out is None:
+        q_out = torch.empty((padded, width), dtype=torch.bfloat16, device=q.device)
+    if k_out is None:
+        k_out = torch.empty((padded, width), dtype=torch.bfloat16, device=q.device)
+    qos, kos = _rows(q_out, "q_out"), _rows(k_out, "k_out")
+    if qos != kos or q_out.shape[0] != k_out.shape[0]:
+        raise ValueError("q_out and k_out must have the same rows and row stride")
+    _check(load().tfk_qk_rmsnorm_rope_neox_fixed_valid(
+        _ptr(q), _ptr(k), qs, _ptr(q_out), _ptr(k_out), qos, _ptr(q_weight), _ptr(k_weight), _ptr(positions),
+        valid_rows, q_out.shape[0], n_heads, head_dim, theta, eps, _stream(q, stream)))
     return q_out, k_out
 
 

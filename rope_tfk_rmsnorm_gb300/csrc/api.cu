@@ -200,12 +200,18 @@ tfk_status tfk_debug_fail_next_launch(int32_t cuda_error) {
     return ok();
 }
 
-tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
-                                     int64_t y_row_stride, const float* weight, const float* shift,
-                                     const float* scale, const int32_t* mod_idx, int32_t n_mod,
-                                     int64_t rows, int32_t hidden, float eps, void* stream) {
-    static const char* op = "tfk_rmsnorm_adaln_indexed";
-    if (rows < 0) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: rows = %lld < 0", op, (long long)rows);
+}  // extern "C"
+
+namespace {
+
+// rows are computed from x; rows [rows, padded_rows) of y are written +0.0.
+tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
+                      int64_t y_row_stride, const float* weight, const float* shift, const float* scale,
+                      const int32_t* mod_idx, int32_t n_mod, int64_t rows, int64_t padded_rows,
+                      int32_t hidden, float eps, void* stream) {
+    if (rows < 0 || padded_rows < rows)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: need 0 <= rows (%lld) <= padded rows (%lld)", op,
+                    (long long)rows, (long long)padded_rows);
     if (hidden <= 0) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: hidden = %d <= 0", op, hidden);
     if (n_mod < 1) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: n_mod = %d < 1", op, n_mod);
     if (!finite_nonneg(eps)) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: eps must be finite and >= 0", op);
@@ -214,8 +220,8 @@ tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride, tf
     if (x_row_stride < hidden || y_row_stride < hidden)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: row strides (%lld, %lld) must be >= hidden %d", op,
                     (long long)x_row_stride, (long long)y_row_stride, hidden);
-    if (rows == 0) return ok();
-    if (!x || !y || !weight || !shift || !scale || !mod_idx)
+    if (padded_rows == 0) return ok();
+    if (!y || (rows > 0 && (!x || !weight || !shift || !scale || !mod_idx)))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: null pointer", op);
     if (x_row_stride % 8 || y_row_stride % 8)
         return fail(TFK_ERR_MISALIGNED, "%s: row strides must be multiples of 8 elements", op);
@@ -223,26 +229,27 @@ tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride, tf
         !aligned(scale, 16) || !aligned(mod_idx, 4))
         return fail(TFK_ERR_MISALIGNED, "%s: x, y, weight, shift, scale need 16-byte and mod_idx 4-byte alignment", op);
     if (!same_region(x, x_row_stride, y, y_row_stride) &&
-        regions_overlap(x, x_row_stride, hidden, y, y_row_stride, hidden, rows, 2))
+        regions_overlap(x, x_row_stride, hidden, y, y_row_stride, hidden, padded_rows, 2))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: y overlaps x without being the same buffer", op);
-    const int64_t ybytes = extent_bytes(rows, y_row_stride, hidden, 2);
+    const int64_t ybytes = extent_bytes(padded_rows, y_row_stride, hidden, 2);
     const int64_t mbytes = (int64_t)n_mod * hidden * 4;
     if (ranges_overlap(y, ybytes, weight, (int64_t)hidden * 4) || ranges_overlap(y, ybytes, shift, mbytes) ||
         ranges_overlap(y, ybytes, scale, mbytes) || ranges_overlap(y, ybytes, mod_idx, rows * 4))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: y overlaps a parameter buffer", op);
     tfk_status st;
     if (take_injected(op, &st)) return st;
-    tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, hidden, eps};
+    tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, padded_rows,
+                     hidden, eps};
     return finish_launch(op, tfk::launch_rmsnorm_adaln(a, static_cast<cudaStream_t>(stream)));
 }
 
-tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
-                                    tfk_bf16* q_out, tfk_bf16* k_out, int64_t out_row_stride,
-                                    const float* q_weight, const float* k_weight,
-                                    const int32_t* positions, int64_t rows, int32_t n_heads,
-                                    int32_t head_dim, float theta, float eps, void* stream) {
-    static const char* op = "tfk_qk_rmsnorm_rope_neox";
-    if (rows < 0) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: rows = %lld < 0", op, (long long)rows);
+tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
+                   tfk_bf16* q_out, tfk_bf16* k_out, int64_t out_row_stride, const float* q_weight,
+                   const float* k_weight, const int32_t* positions, int64_t rows, int64_t padded_rows,
+                   int32_t n_heads, int32_t head_dim, float theta, float eps, void* stream) {
+    if (rows < 0 || padded_rows < rows)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: need 0 <= rows (%lld) <= padded rows (%lld)", op,
+                    (long long)rows, (long long)padded_rows);
     if (n_heads < 1 || head_dim < 1)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: n_heads = %d, head_dim = %d", op, n_heads, head_dim);
     if (!finite_nonneg(eps)) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: eps must be finite and >= 0", op);
@@ -255,8 +262,8 @@ tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_
     if (in_row_stride < width || out_row_stride < width)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: row strides (%lld, %lld) must be >= n_heads*head_dim = %lld",
                     op, (long long)in_row_stride, (long long)out_row_stride, (long long)width);
-    if (rows == 0) return ok();
-    if (!q || !k || !q_out || !k_out || !q_weight || !k_weight || !positions)
+    if (padded_rows == 0) return ok();
+    if (!q_out || !k_out || (rows > 0 && (!q || !k || !q_weight || !k_weight || !positions)))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: null pointer", op);
     if (in_row_stride % 8 || out_row_stride % 8)
         return fail(TFK_ERR_MISALIGNED, "%s: row strides must be multiples of 8 elements", op);
@@ -264,16 +271,17 @@ tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_
         !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(positions, 4))
         return fail(TFK_ERR_MISALIGNED, "%s: q, k, outputs and weights need 16-byte, positions 4-byte alignment", op);
     const int64_t is = in_row_stride, os = out_row_stride;
-    if (regions_overlap(q_out, os, width, k_out, os, width, rows, 2))
+    const int64_t orows = padded_rows;  // rows of the outputs that are written
+    if (regions_overlap(q_out, os, width, k_out, os, width, orows, 2))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: q_out and k_out overlap", op);
-    if (!same_region(q, is, q_out, os) && regions_overlap(q, is, width, q_out, os, width, rows, 2))
+    if (!same_region(q, is, q_out, os) && regions_overlap(q, is, width, q_out, os, width, orows, 2))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: q_out overlaps q without being the same buffer", op);
-    if (!same_region(k, is, k_out, os) && regions_overlap(k, is, width, k_out, os, width, rows, 2))
+    if (!same_region(k, is, k_out, os) && regions_overlap(k, is, width, k_out, os, width, orows, 2))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: k_out overlaps k without being the same buffer", op);
-    if (regions_overlap(q, is, width, k_out, os, width, rows, 2) ||
-        regions_overlap(k, is, width, q_out, os, width, rows, 2))
+    if (regions_overlap(q, is, width, k_out, os, width, orows, 2) ||
+        regions_overlap(k, is, width, q_out, os, width, orows, 2))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: an output overlaps the other tensor's input", op);
-    const int64_t ob = extent_bytes(rows, os, width, 2);
+    const int64_t ob = extent_bytes(orows, os, width, 2);
     const int64_t wb = (int64_t)head_dim * 4;
     if (ranges_overlap(q_out, ob, q_weight, wb) || ranges_overlap(q_out, ob, k_weight, wb) ||
         ranges_overlap(k_out, ob, q_weight, wb) || ranges_overlap(k_out, ob, k_weight, wb) ||
@@ -282,8 +290,48 @@ tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_
     tfk_status st;
     if (take_injected(op, &st)) return st;
     tfk::QkRopeArgs a{q, k, in_row_stride, q_out, k_out, out_row_stride, q_weight, k_weight,
-                      positions, rows, n_heads, head_dim, theta, eps};
+                      positions, rows, padded_rows, n_heads, head_dim, theta, eps};
     return finish_launch(op, tfk::launch_qk_rmsnorm_rope(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
+                                     int64_t y_row_stride, const float* weight, const float* shift,
+                                     const float* scale, const int32_t* mod_idx, int32_t n_mod,
+                                     int64_t rows, int32_t hidden, float eps, void* stream) {
+    return adaln_impl("tfk_rmsnorm_adaln_indexed", x, x_row_stride, y, y_row_stride, weight, shift, scale,
+                      mod_idx, n_mod, rows, rows, hidden, eps, stream);
+}
+
+tfk_status tfk_rmsnorm_adaln_indexed_fixed_valid(const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
+                                                 int64_t y_row_stride, const float* weight, const float* shift,
+                                                 const float* scale, const int32_t* mod_idx, int32_t n_mod,
+                                                 int64_t valid_rows, int64_t padded_rows, int32_t hidden,
+                                                 float eps, void* stream) {
+    return adaln_impl("tfk_rmsnorm_adaln_indexed_fixed_valid", x, x_row_stride, y, y_row_stride, weight, shift,
+                      scale, mod_idx, n_mod, valid_rows, padded_rows, hidden, eps, stream);
+}
+
+tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
+                                    tfk_bf16* q_out, tfk_bf16* k_out, int64_t out_row_stride,
+                                    const float* q_weight, const float* k_weight,
+                                    const int32_t* positions, int64_t rows, int32_t n_heads,
+                                    int32_t head_dim, float theta, float eps, void* stream) {
+    return qk_impl("tfk_qk_rmsnorm_rope_neox", q, k, in_row_stride, q_out, k_out, out_row_stride, q_weight,
+                   k_weight, positions, rows, rows, n_heads, head_dim, theta, eps, stream);
+}
+
+tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
+                                                tfk_bf16* q_out, tfk_bf16* k_out, int64_t out_row_stride,
+                                                const float* q_weight, const float* k_weight,
+                                                const int32_t* positions, int64_t valid_rows,
+                                                int64_t padded_rows, int32_t n_heads, int32_t head_dim,
+                                                float theta, float eps, void* stream) {
+    return qk_impl("tfk_qk_rmsnorm_rope_neox_fixed_valid", q, k, in_row_stride, q_out, k_out, out_row_stride,
+                   q_weight, k_weight, positions, valid_rows, padded_rows, n_heads, head_dim, theta, eps, stream);
 }
 
 tfk_status tfk_swiglu(const tfk_bf16* gate_up, int64_t in_row_stride, tfk_bf16* out,

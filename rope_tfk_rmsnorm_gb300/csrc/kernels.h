@@ -25,7 +25,8 @@ struct AdalnArgs {
     const float* shift;
     const float* scale;
     const int32_t* mod_idx;
-    int64_t rows;
+    int64_t rows;         // rows computed from x
+    int64_t padded_rows;  // rows [rows, padded_rows) of y are written +0.0 (== rows: none)
     int hidden;
     float eps;
 };
@@ -41,7 +42,8 @@ struct QkRopeArgs {
     const float* q_weight;
     const float* k_weight;
     const int32_t* pos;
-    int64_t rows;
+    int64_t rows;         // rows computed from q, k
+    int64_t padded_rows;  // rows [rows, padded_rows) of q_out, k_out are written +0.0
     int n_heads;
     int head_dim;
     float theta;

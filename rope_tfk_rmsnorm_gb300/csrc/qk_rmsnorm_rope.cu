@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(kMaxThreads) qk_rope_kernel(const QkRopeArgs a
 
     const int64_t r0 = a.rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = a.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
-    if (r0 >= r1) return;  // uniform over the CTA
     const int nrows = (int)(r1 - r0);
 
     // Fixed-point turn fractions of the D/2 frequencies.  Thread tid owns the
@@ -116,6 +115,7 @@ __global__ void __launch_bounds__(kMaxThreads) qk_rope_kernel(const QkRopeArgs a
         }
     };
 
+    if (nrows > 0) {  // uniform over the CTA
     for (int s = 0; s < stages - 1; ++s) {
         if (s < nrows) issue(s, s);
         cp_async_commit();
@@ -170,6 +170,27 @@ __global__ void __launch_bounds__(kMaxThreads) qk_rope_kernel(const QkRopeArgs a
         }
     }
     cp_async_wait<0>();
+    }  // nrows > 0
+
+    // Fixed-valid mode: this CTA's share of the padded tail rows of q_out and
+    // k_out is written +0.0 in the same launch (the input tail is never read).
+    const int64_t tail = a.padded_rows - a.rows;
+    if (tail > 0) {
+        const int64_t z0 = a.rows + tail * (int64_t)blockIdx.x / gridDim.x;
+        const int64_t z1 = a.rows + tail * (int64_t)(blockIdx.x + 1) / gridDim.x;
+        Vec8 zero;
+        zero.w[0] = zero.w[1] = zero.w[2] = zero.w[3] = 0u;
+        for (int64_t r = z0; r < z1; ++r) {
+            const int64_t roff = r * a.out_stride;
+#pragma unroll
+            for (int j = 0; j < HPT; ++j) {
+                if (active[j]) {
+                    st_vec(dst0[j] + roff, zero);
+                    st_vec(dst0[j] + roff + half, zero);
+                }
+            }
+        }
+    }
 }
 
 struct Shape {
@@ -209,7 +230,9 @@ cudaError_t launch_h(const QkRopeArgs& a, const Shape& s, cudaStream_t stream) {
     const int per_sm = blocks_per_sm(fn, s.threads, smem);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)per_sm * di.sm_count;
-    if (grid > a.rows) grid = a.rows;
+    const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
+    if (grid > work) grid = work;
+    if (grid < 1) return cudaSuccess;
     qk_rope_kernel<HPT><<<(unsigned)grid, s.threads, smem, stream>>>(a, s.lanes, stages);
     return cudaGetLastError();
 }

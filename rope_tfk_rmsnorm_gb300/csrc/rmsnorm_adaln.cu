@@ -62,7 +62,6 @@ __global__ void __launch_bounds__(kMaxThreads) rmsnorm_adaln_kernel(const AdalnA
 
     const int64_t r0 = a.rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = a.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
-    if (r0 >= r1) return;  // uniform over the CTA
     const int nrows = (int)(r1 - r0);
 
     int col[V];
@@ -82,6 +81,7 @@ __global__ void __launch_bounds__(kMaxThreads) rmsnorm_adaln_kernel(const AdalnA
         }
     }
 
+    if (nrows > 0) {  // uniform over the CTA
     // Prologue: rows 0 .. stages-2 of this CTA's run go in flight.
     for (int s = 0; s < stages - 1; ++s) {
         if (s < nrows) {
@@ -179,6 +179,23 @@ __global__ void __launch_bounds__(kMaxThreads) rmsnorm_adaln_kernel(const AdalnA
         }
     }
     cp_async_wait<0>();
+    }  // nrows > 0
+
+    // Fixed-valid mode: this CTA's share of the padded tail is written +0.0
+    // in the same launch (stores only; the tail of x is never read).
+    const int64_t tail = a.padded_rows - a.rows;
+    if (tail > 0) {
+        const int64_t z0 = a.rows + tail * (int64_t)blockIdx.x / gridDim.x;
+        const int64_t z1 = a.rows + tail * (int64_t)(blockIdx.x + 1) / gridDim.x;
+        Vec8 zero;
+        zero.w[0] = zero.w[1] = zero.w[2] = zero.w[3] = 0u;
+        for (int64_t r = z0; r < z1; ++r) {
+            uint16_t* dst = a.y + r * a.y_stride;
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (ok[i]) st_vec(dst + col[i] * 8, zero);
+        }
+    }
 }
 
 bool choose_shape(int hidden, int* v, int* threads) {
@@ -208,7 +225,9 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     const int per_sm = blocks_per_sm(fn, threads, smem);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)per_sm * di.sm_count;
-    if (grid > a.rows) grid = a.rows;
+    const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
+    if (grid > work) grid = work;
+    if (grid < 1) return cudaSuccess;
     rmsnorm_adaln_kernel<V><<<(unsigned)grid, threads, smem, stream>>>(a, stages);
     return cudaGetLastError();
 }

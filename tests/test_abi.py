@@ -57,7 +57,7 @@ def passes_validation(lib, call):
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert len(names) == 10, names
+    assert len(names) == 12, names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in tfk.h but not exported"
     assert sorted(n for n, _, _ in tfk.SIGNATURES) == names
@@ -174,3 +174,20 @@ def test_python_binding_rejects_bad_tensors_before_the_abi():
     xb = torch.zeros(4, 16, dtype=torch.bfloat16)   # CPU tensor: the library has no CPU path
     with pytest.raises(ValueError, match="CUDA"):
         tfk.tfk_swiglu(xb)
+
+
+def test_fixed_valid_validation(lib):
+    fa = lambda L=10, N=16, x=A, y=B, idx=P: lib.tfk_rmsnorm_adaln_indexed_fixed_valid(
+        x, 512, y, 512, W, S, S + 0x100000, idx, 2, L, N, 512, 1e-6, None)
+    assert passes_validation(lib, fa)
+    assert passes_validation(lib, lambda: fa(L=0, x=0, idx=0))              # the whole buffer becomes +0.0
+    assert passes_validation(lib, lambda: fa(y=A))                          # in place
+    assert fa(L=0, N=0, x=0, y=0, idx=0) == OK
+    assert fa(L=17, N=16) == INVALID and fa(L=-1) == INVALID
+    assert fa(y=0) == INVALID
+    assert fa(y=A + 512 * 2 * 12) == INVALID                                # y's padded rows reach into x
+    fq = lambda L=10, N=16, qo=B, ko=B + 2 * 1024: lib.tfk_qk_rmsnorm_rope_neox_fixed_valid(
+        A, A + 2 * 1024, 3 * 1024, qo, ko, 3 * 1024, W, W + 64, P, L, N, 8, 128, 10000.0, 1e-6, None)
+    assert passes_validation(lib, fq)
+    assert passes_validation(lib, lambda: fq(qo=A, ko=A + 2 * 1024))
+    assert fq(L=20) == INVALID and fq(ko=B + 1024) == INVALID

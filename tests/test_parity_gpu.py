@@ -476,3 +476,65 @@ def test_over_2g_elements_indexing(cuda):
     assert torch.equal(padded[idx].view(torch.int16), comp[idx].view(torch.int16))
     del gu, comp, padded
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# fixed-valid mode: the normalisation kernels on the padded buffer directly
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,L", [(64, 0), (64, 64), (1000, 777), (4096, 1)])
+def test_fixed_valid_adaln_and_qk(cuda, N, L):
+    rng = np.random.default_rng(N + 3 * L)
+    hidden, H, D = 1024, 8, 128
+    x = rand_bits(rng, (N, hidden))
+    q = rand_bits(rng, (N, H * D), 2.0)
+    k = rand_bits(rng, (N, H * D))
+    for a in (x, q, k):
+        a[L:] = synth.BF16_NAN                        # the padded tail must never be read
+    w, sh, sc = mod_params(rng, 3, hidden)
+    idx = rng.integers(0, 3, L).astype(np.int32)
+    pos = rng.integers(0, 70000, L).astype(np.int32)
+    wq = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+
+    y = Guarded(N, hidden)
+    tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(to_dev(x), L, f32_dev(w), f32_dev(sh), f32_dev(sc), i32_dev(idx),
+                                              1e-6, out=y.view)
+    qo, ko = Guarded(N, H * D), Guarded(N, H * D)
+    tfk.tfk_qk_rmsnorm_rope_neox_fixed_valid(to_dev(q), to_dev(k), L, f32_dev(wq), f32_dev(wk), i32_dev(pos),
+                                             H, D, 10000.0, 1e-6, q_out=qo.view, k_out=ko.view)
+    torch.cuda.synchronize()
+    for g in (y, qo, ko):
+        g.check()
+        assert np.all(g.host()[L:] == 0x0000)
+    check_close(y.host(), oracle.rmsnorm_adaln_fixed_valid(x, L, w, sh, sc, idx, 1e-6, threads=THREADS),
+                "fixed-valid a1")
+    rq, rk = oracle.qk_rmsnorm_rope_neox_fixed_valid(q, k, L, wq, wk, pos, H, D, 10000.0, 1e-6, threads=THREADS)
+    check_close(qo.host(), rq.reshape(N, -1), "fixed-valid q")
+    check_close(ko.host(), rk.reshape(N, -1), "fixed-valid k")
+
+
+def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
+    """The valid-only workload without gather and merge: in place on the padded buffers."""
+    wl = synth.get("valid_only")
+    N, L = wl.rows, synth.valid_len(wl)
+    host, dev = _inputs_dev(wl, ["x", "q", "k"])
+    p, pd = _params_dev(wl)
+    idx = synth.mod_index(wl, np.arange(L))
+    pos = synth.positions(wl, np.arange(L))
+    tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(dev["x"], L, pd["w"], pd["shift"], pd["scale"], i32_dev(idx),
+                                              wl.eps, out=dev["x"])
+    tfk.tfk_qk_rmsnorm_rope_neox_fixed_valid(dev["q"], dev["k"], L, pd["w_q"], pd["w_k"], i32_dev(pos),
+                                             wl.n_heads, wl.head_dim, wl.theta, wl.eps,
+                                             q_out=dev["q"], k_out=dev["k"])
+    torch.cuda.synchronize()
+    y, qo, ko = (to_host(dev[t]) for t in ("x", "q", "k"))
+    for a in (y, qo, ko):
+        assert np.all(a[L:] == 0x0000)
+    sample = synth.sample_rows(wl, 256, limit=L)
+    check_close(y[sample], ora_adaln(host["x"][sample], p["w"], p["shift"], p["scale"], idx[sample], wl.eps),
+                "valid-only fixed-valid a1")
+    rq, rk = ora_qk(host["q"][sample], host["k"][sample], p["w_q"], p["w_k"], pos[sample], wl.n_heads,
+                    wl.head_dim, wl.theta, wl.eps)
+    check_close(qo[sample], rq, "valid-only fixed-valid q")
+    check_close(ko[sample], rk, "valid-only fixed-valid k")
