@@ -157,6 +157,45 @@ tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf1
                                                 void* stream);
 
 /*
+ * Q/K RMSNorm + NeoX RoPE fused with Ulysses packing ("Fuse Q/K RMSNorm, RoPE,
+ * and Ulysses packing", TeleFuser PR #38 section 2): the same arithmetic as
+ * tfk_qk_rmsnorm_rope_neox, stored directly in the send layout of the
+ * Ulysses sequence-parallel all-to-all of degree P = sp_degree:
+ *
+ *   q_send[p][t][j][d] = out_q[t][p*H/P + j][d]     (same for k)
+ *
+ * so block p (rows*H/P*D contiguous values) is what rank p receives.
+ * q_send, k_send  contiguous [P, rows, n_heads/P, head_dim] bf16; must not
+ *                 overlap any input.  P >= 1 and P divides n_heads; P == 1 is
+ *                 the plain contiguous [rows, n_heads*head_dim] layout.
+ * Other arguments and limits as for tfk_qk_rmsnorm_rope_neox.
+ */
+tfk_status tfk_qk_rmsnorm_rope_neox_ulysses(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
+                                            tfk_bf16* q_send, tfk_bf16* k_send,
+                                            const float* q_weight, const float* k_weight,
+                                            const int32_t* positions, int64_t rows,
+                                            int32_t n_heads, int32_t head_dim, int32_t sp_degree,
+                                            float theta, float eps, void* stream);
+
+/*
+ * Ulysses head <-> sequence relayout ("Ulysses relayout", TeleFuser PR #23
+ * "Changes Made"), a bit-exact permutation around the all-to-all:
+ *
+ *   pack:    dst[p][t][j][d] = src[t][(p*H/P + j)*D + d]
+ *   unpack:  dst[t][(p*H/P + j)*D + d] = src[p][t][j][d]
+ *
+ * The row-layout side is [rows, row_stride] bf16 (H = n_heads heads of
+ * D = head_dim values per row, row_stride >= H*D, a multiple of 8); the
+ * grouped side is contiguous [P, rows, H/P, D].  head_dim a multiple of 8;
+ * P = sp_degree >= 1 divides n_heads.  Source and destination must not overlap.
+ */
+tfk_status tfk_ulysses_pack(const tfk_bf16* src, int64_t src_row_stride, tfk_bf16* dst, int64_t rows,
+                            int32_t n_heads, int32_t head_dim, int32_t sp_degree, void* stream);
+
+tfk_status tfk_ulysses_unpack(const tfk_bf16* src, tfk_bf16* dst, int64_t dst_row_stride, int64_t rows,
+                              int32_t n_heads, int32_t head_dim, int32_t sp_degree, void* stream);
+
+/*
  * SwiGLU on the FFN up-projection output ("SwiGLU", TeleFuser PR #23
  * "Changes Made"):
  *

@@ -258,3 +258,20 @@ def qk_rmsnorm_rope_neox_fixed_valid(q_padded, k_padded, valid_rows: int, q_weig
                                                             q_weight, k_weight, np.asarray(pos)[:valid_rows],
                                                             n_heads, head_dim, base, eps, threads=threads)
     return qo, ko
+
+
+# ---- Ulysses relayout ("Ulysses relayout", TeleFuser PR #23; packing fused into Q/K
+#      RMSNorm + RoPE, TeleFuser PR #38 section 2) ----
+
+def ulysses_pack(rows_layout: np.ndarray, n_heads: int, head_dim: int, sp_degree: int) -> np.ndarray:
+    """[rows, n_heads*head_dim] -> [sp_degree, rows, n_heads/sp_degree, head_dim]: block p holds the
+    heads p*H/P .. (p+1)*H/P - 1 of every row, the block that sequence-parallel rank p receives."""
+    rows = rows_layout.shape[0]
+    a = np.asarray(rows_layout)[:, :n_heads * head_dim].reshape(rows, sp_degree, n_heads // sp_degree, head_dim)
+    return np.ascontiguousarray(a.transpose(1, 0, 2, 3))
+
+
+def ulysses_unpack(grouped: np.ndarray, n_heads: int, head_dim: int, sp_degree: int) -> np.ndarray:
+    """Inverse of ulysses_pack: [sp_degree, rows, n_heads/sp_degree, head_dim] -> [rows, n_heads*head_dim]."""
+    g = np.asarray(grouped).reshape(sp_degree, -1, n_heads // sp_degree, head_dim)
+    return np.ascontiguousarray(g.transpose(1, 0, 2, 3)).reshape(g.shape[1], n_heads * head_dim)

@@ -37,6 +37,10 @@ SIGNATURES = [
      [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _f32, _vp]),
     ("tfk_qk_rmsnorm_rope_neox_fixed_valid", ctypes.c_int,
      [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _f32, _f32, _vp]),
+    ("tfk_qk_rmsnorm_rope_neox_ulysses", ctypes.c_int,
+     [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _f32, _f32, _vp]),
+    ("tfk_ulysses_pack", ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _i32, _vp]),
+    ("tfk_ulysses_unpack", ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp]),
     ("tfk_swiglu", ctypes.c_int, [_vp, _i64, _vp, _i64, _i64, _i32, _vp]),
     ("tfk_valid_gather", ctypes.c_int, [_vp, _vp, _i64, _i32, _vp]),
     ("tfk_zero_tail_merge", ctypes.c_int, [_vp, _vp, _i64, _i64, _i32, _vp]),
@@ -198,6 +202,62 @@ def tfk_qk_rmsnorm_rope_neox_fixed_valid(q: torch.Tensor, k: torch.Tensor, valid
         _ptr(q), _ptr(k), qs, _ptr(q_out), _ptr(k_out), qos, _ptr(q_weight), _ptr(k_weight), _ptr(positions),
         valid_rows, q_out.shape[0], n_heads, head_dim, theta, eps, _stream(q, stream)))
     return q_out, k_out
+
+
+def tfk_qk_rmsnorm_rope_neox_ulysses(q: torch.Tensor, k: torch.Tensor, q_weight: torch.Tensor,
+                                     k_weight: torch.Tensor, positions: torch.Tensor, n_heads: int,
+                                     head_dim: int, sp_degree: int, theta: float = 10000.0, eps: float = 1e-6,
+                                     q_send: torch.Tensor | None = None, k_send: torch.Tensor | None = None,
+                                     stream=None):
+    """Q/K RMSNorm + RoPE written into Ulysses send buffers [sp_degree, rows, n_heads/sp_degree, head_dim]."""
+    qs, ks = _rows(q, "q"), _rows(k, "k")
+    if qs != ks or q.shape[0] != k.shape[0]:
+        raise ValueError("q and k must have the same rows and row stride")
+    rows = q.shape[0]
+    shape = (sp_degree, rows, n_heads // max(1, sp_degree), head_dim)
+    _param(q_weight, "q_weight")
+    _param(k_weight, "k_weight")
+    _param(positions, "positions", torch.int32)
+    if q_send is None:
+        q_send = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if k_send is None:
+        k_send = torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    for t, n in ((q_send, "q_send"), (k_send, "k_send")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.numel() != rows * n_heads * head_dim:
+            raise ValueError(f"{n} must be a contiguous CUDA bf16 tensor of {shape}")
+    _check(load().tfk_qk_rmsnorm_rope_neox_ulysses(_ptr(q), _ptr(k), qs, _ptr(q_send), _ptr(k_send), _ptr(q_weight),
+                                                   _ptr(k_weight), _ptr(positions), rows, n_heads, head_dim,
+                                                   sp_degree, theta, eps, _stream(q, stream)))
+    return q_send, k_send
+
+
+def tfk_ulysses_pack(src: torch.Tensor, n_heads: int, head_dim: int, sp_degree: int,
+                     dst: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """[rows, >= n_heads*head_dim] -> contiguous [sp_degree, rows, n_heads/sp_degree, head_dim]."""
+    ss = _rows(src, "src")
+    rows = src.shape[0]
+    if dst is None:
+        dst = torch.empty((sp_degree, rows, n_heads // max(1, sp_degree), head_dim), dtype=torch.bfloat16,
+                          device=src.device)
+    if dst.dtype != torch.bfloat16 or not dst.is_contiguous() or dst.numel() != rows * n_heads * head_dim:
+        raise ValueError("dst must be a contiguous bf16 tensor of rows*n_heads*head_dim elements")
+    _check(load().tfk_ulysses_pack(_ptr(src), ss, _ptr(dst), rows, n_heads, head_dim, sp_degree,
+                                   _stream(src, stream)))
+    return dst
+
+
+def tfk_ulysses_unpack(src: torch.Tensor, n_heads: int, head_dim: int, sp_degree: int,
+                       dst: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Contiguous [sp_degree, rows, n_heads/sp_degree, head_dim] -> [rows, n_heads*head_dim] (or dst's stride)."""
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA bf16 tensor")
+    rows = src.numel() // (n_heads * head_dim)
+    if dst is None:
+        dst = torch.empty((rows, n_heads * head_dim), dtype=torch.bfloat16, device=src.device)
+    ds = _rows(dst, "dst")
+    _check(load().tfk_ulysses_unpack(_ptr(src), _ptr(dst), ds, rows, n_heads, head_dim, sp_degree,
+                                     _stream(src, stream)))
+    return dst
 
 
 def tfk_swiglu(gate_up: torch.Tensor, out: torch.Tensor | None = None, ffn: int | None = None,

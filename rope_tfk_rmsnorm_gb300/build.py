@@ -19,7 +19,7 @@ OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtfk.so")
 
 SOURCES = ["api.cu", "rmsnorm_adaln.cu", "qk_rmsnorm_rope.cu", "swiglu.cu", "gather_merge.cu",
-           "velocity_cache.cpp"]
+           "ulysses.cu", "velocity_cache.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

@@ -76,13 +76,23 @@ int blocks_per_sm(const void* func, int threads, size_t smem) {
             if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
             di.max_smem_per_block_optin = optin;
         }
-        if ((int64_t)smem > di.max_smem_per_block_optin) return 0;
-        if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 di.max_smem_per_block_optin) != cudaSuccess)
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
+            cudaGetLastError();  // leave no stale error for the next launch check
             return 0;
+        }
+        const int64_t dyn_max = (int64_t)di.max_smem_per_block_optin - (int64_t)fa.sharedSizeBytes;
+        if ((int64_t)smem > dyn_max) return 0;
+        if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_max) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
     }
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, func, threads, smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, func, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
     if (g_occ_n < kOccEntries) g_occ[g_occ_n++] = OccEntry{dev, func, threads, smem, blocks};
     return blocks;
 }
@@ -94,10 +104,10 @@ int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes) {
     int ahead = (kInflightPerSm + ctas_per_sm * stage_bytes - 1) / (ctas_per_sm * stage_bytes);
     int stages = ahead + 1;
     if (stages > 16) stages = 16;
-    // shared memory per SM (1 KB reserved per CTA) and per CTA
-    const int64_t per_sm_budget = di.max_smem_per_sm / ctas_per_sm - 1024 - 512;
+    // shared memory per SM (1 KB reserved per CTA) and per CTA (1 KB left for static shared memory)
+    const int64_t per_sm_budget = di.max_smem_per_sm / ctas_per_sm - 1024 - 1024;
     while (stages > 2 && ((int64_t)stages * stage_bytes + extra_bytes > per_sm_budget ||
-                          (int64_t)stages * stage_bytes + extra_bytes > di.max_smem_per_block_optin))
+                          (int64_t)stages * stage_bytes + extra_bytes > di.max_smem_per_block_optin - 1024))
         --stages;
     return stages < 2 ? 2 : stages;
 }
@@ -120,6 +130,11 @@ tfk_status fail(tfk_status s, const char* fmt, ...) {
 }
 
 tfk_status ok() { return TFK_OK; }
+
+// Launches go through the library's own (static) CUDA runtime, whose
+// last-error state only this library touches: clear it before a launch so
+// that the check after the launch reports that launch alone.
+void clear_stale_error() { cudaGetLastError(); }
 
 tfk_status finish_launch(const char* op, cudaError_t err) {
     if (err != cudaSuccess)
@@ -238,15 +253,19 @@ tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, t
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: y overlaps a parameter buffer", op);
     tfk_status st;
     if (take_injected(op, &st)) return st;
+    clear_stale_error();
     tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, padded_rows,
                      hidden, eps};
     return finish_launch(op, tfk::launch_rmsnorm_adaln(a, static_cast<cudaStream_t>(stream)));
 }
 
+// sp_degree == 0: outputs are [padded_rows, out_row_stride] row layouts.
+// sp_degree >= 1: outputs are contiguous Ulysses send buffers [sp][rows][n_heads/sp][head_dim].
 tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
                    tfk_bf16* q_out, tfk_bf16* k_out, int64_t out_row_stride, const float* q_weight,
                    const float* k_weight, const int32_t* positions, int64_t rows, int64_t padded_rows,
-                   int32_t n_heads, int32_t head_dim, float theta, float eps, void* stream) {
+                   int32_t n_heads, int32_t head_dim, float theta, float eps, int32_t sp_degree,
+                   void* stream) {
     if (rows < 0 || padded_rows < rows)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: need 0 <= rows (%lld) <= padded rows (%lld)", op,
                     (long long)rows, (long long)padded_rows);
@@ -258,8 +277,11 @@ tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t
     if (head_dim % 16 != 0 || !tfk::qk_rope_supported(n_heads, head_dim))
         return fail(TFK_ERR_UNSUPPORTED, "%s: head_dim = %d, n_heads = %d not supported (head_dim a multiple "
                     "of 16 in [16, 512]; 2*n_heads*pow2(head_dim/16) <= 2048)", op, head_dim, n_heads);
+    if (sp_degree < 0 || (sp_degree > 0 && n_heads % sp_degree != 0))
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: sp_degree %d must divide n_heads %d", op, sp_degree, n_heads);
     const int64_t width = (int64_t)n_heads * head_dim;
-    if (in_row_stride < width || out_row_stride < width)
+    if (sp_degree > 0) out_row_stride = width / sp_degree;  // row pitch inside one send block
+    if (in_row_stride < width || (sp_degree == 0 && out_row_stride < width))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: row strides (%lld, %lld) must be >= n_heads*head_dim = %lld",
                     op, (long long)in_row_stride, (long long)out_row_stride, (long long)width);
     if (padded_rows == 0) return ok();
@@ -272,6 +294,15 @@ tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t
         return fail(TFK_ERR_MISALIGNED, "%s: q, k, outputs and weights need 16-byte, positions 4-byte alignment", op);
     const int64_t is = in_row_stride, os = out_row_stride;
     const int64_t orows = padded_rows;  // rows of the outputs that are written
+    if (sp_degree > 0) {  // contiguous send buffers: byte ranges against everything else
+        const int64_t sb = rows * width * 2, ib = extent_bytes(rows, is, width, 2);
+        if (ranges_overlap(q_out, sb, k_out, sb) || ranges_overlap(q_out, sb, q, ib) ||
+            ranges_overlap(q_out, sb, k, ib) || ranges_overlap(k_out, sb, q, ib) || ranges_overlap(k_out, sb, k, ib) ||
+            ranges_overlap(q_out, sb, q_weight, head_dim * 4) || ranges_overlap(q_out, sb, k_weight, head_dim * 4) ||
+            ranges_overlap(k_out, sb, q_weight, head_dim * 4) || ranges_overlap(k_out, sb, k_weight, head_dim * 4) ||
+            ranges_overlap(q_out, sb, positions, rows * 4) || ranges_overlap(k_out, sb, positions, rows * 4))
+            return fail(TFK_ERR_INVALID_ARGUMENT, "%s: a send buffer overlaps another buffer", op);
+    } else {
     if (regions_overlap(q_out, os, width, k_out, os, width, orows, 2))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: q_out and k_out overlap", op);
     if (!same_region(q, is, q_out, os) && regions_overlap(q, is, width, q_out, os, width, orows, 2))
@@ -287,10 +318,14 @@ tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t
         ranges_overlap(k_out, ob, q_weight, wb) || ranges_overlap(k_out, ob, k_weight, wb) ||
         ranges_overlap(q_out, ob, positions, rows * 4) || ranges_overlap(k_out, ob, positions, rows * 4))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: an output overlaps a weight or the positions", op);
+    }
     tfk_status st;
     if (take_injected(op, &st)) return st;
+    clear_stale_error();
+    const int hpg = sp_degree > 0 ? n_heads / sp_degree : n_heads;
+    const int64_t gstride = sp_degree > 0 ? rows * hpg * (int64_t)head_dim : 0;
     tfk::QkRopeArgs a{q, k, in_row_stride, q_out, k_out, out_row_stride, q_weight, k_weight,
-                      positions, rows, padded_rows, n_heads, head_dim, theta, eps};
+                      positions, rows, padded_rows, hpg, gstride, n_heads, head_dim, theta, eps};
     return finish_launch(op, tfk::launch_qk_rmsnorm_rope(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -321,7 +356,7 @@ tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_
                                     const int32_t* positions, int64_t rows, int32_t n_heads,
                                     int32_t head_dim, float theta, float eps, void* stream) {
     return qk_impl("tfk_qk_rmsnorm_rope_neox", q, k, in_row_stride, q_out, k_out, out_row_stride, q_weight,
-                   k_weight, positions, rows, rows, n_heads, head_dim, theta, eps, stream);
+                   k_weight, positions, rows, rows, n_heads, head_dim, theta, eps, 0, stream);
 }
 
 tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
@@ -331,7 +366,58 @@ tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf1
                                                 int64_t padded_rows, int32_t n_heads, int32_t head_dim,
                                                 float theta, float eps, void* stream) {
     return qk_impl("tfk_qk_rmsnorm_rope_neox_fixed_valid", q, k, in_row_stride, q_out, k_out, out_row_stride,
-                   q_weight, k_weight, positions, valid_rows, padded_rows, n_heads, head_dim, theta, eps, stream);
+                   q_weight, k_weight, positions, valid_rows, padded_rows, n_heads, head_dim, theta, eps, 0,
+                   stream);
+}
+
+tfk_status tfk_qk_rmsnorm_rope_neox_ulysses(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,
+                                            tfk_bf16* q_send, tfk_bf16* k_send, const float* q_weight,
+                                            const float* k_weight, const int32_t* positions, int64_t rows,
+                                            int32_t n_heads, int32_t head_dim, int32_t sp_degree, float theta,
+                                            float eps, void* stream) {
+    static const char* op = "tfk_qk_rmsnorm_rope_neox_ulysses";
+    if (sp_degree < 1) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: sp_degree = %d < 1", op, sp_degree);
+    return qk_impl(op, q, k, in_row_stride, q_send, k_send, 0, q_weight, k_weight, positions, rows, rows,
+                   n_heads, head_dim, theta, eps, sp_degree, stream);
+}
+
+static tfk_status relayout_impl(const char* op, const tfk_bf16* src, tfk_bf16* dst, int64_t row_stride,
+                                int64_t rows, int32_t n_heads, int32_t head_dim, int32_t sp_degree, bool pack,
+                                void* stream) {
+    if (rows < 0) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: rows = %lld < 0", op, (long long)rows);
+    if (n_heads < 1 || head_dim < 1 || sp_degree < 1 || n_heads % sp_degree != 0)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: n_heads %d, head_dim %d, sp_degree %d (must divide n_heads)",
+                    op, n_heads, head_dim, sp_degree);
+    if (head_dim % 8 != 0) return fail(TFK_ERR_UNSUPPORTED, "%s: head_dim %d is not a multiple of 8", op, head_dim);
+    const int64_t width = (int64_t)n_heads * head_dim;
+    if (width > (int64_t)1 << 30) return fail(TFK_ERR_UNSUPPORTED, "%s: row too wide", op);
+    if (row_stride < width)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: row stride %lld < n_heads*head_dim", op, (long long)row_stride);
+    if (rows == 0) return ok();
+    if (!src || !dst) return fail(TFK_ERR_INVALID_ARGUMENT, "%s: null pointer", op);
+    if (row_stride % 8 || !aligned(src, 16) || !aligned(dst, 16))
+        return fail(TFK_ERR_MISALIGNED, "%s: 16-byte alignment of pointers and row stride required", op);
+    const void* rowbuf = pack ? (const void*)src : (const void*)dst;
+    const void* grpbuf = pack ? (const void*)dst : (const void*)src;
+    if (ranges_overlap(rowbuf, extent_bytes(rows, row_stride, width, 2), grpbuf, rows * width * 2))
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: source and destination overlap", op);
+    tfk_status st;
+    if (take_injected(op, &st)) return st;
+    clear_stale_error();
+    return finish_launch(op, tfk::launch_ulysses_relayout(src, dst, row_stride, rows, n_heads, head_dim, sp_degree,
+                                                          pack, static_cast<cudaStream_t>(stream)));
+}
+
+tfk_status tfk_ulysses_pack(const tfk_bf16* src, int64_t src_row_stride, tfk_bf16* dst, int64_t rows,
+                            int32_t n_heads, int32_t head_dim, int32_t sp_degree, void* stream) {
+    return relayout_impl("tfk_ulysses_pack", src, dst, src_row_stride, rows, n_heads, head_dim, sp_degree, true,
+                         stream);
+}
+
+tfk_status tfk_ulysses_unpack(const tfk_bf16* src, tfk_bf16* dst, int64_t dst_row_stride, int64_t rows,
+                              int32_t n_heads, int32_t head_dim, int32_t sp_degree, void* stream) {
+    return relayout_impl("tfk_ulysses_unpack", src, dst, dst_row_stride, rows, n_heads, head_dim, sp_degree, false,
+                         stream);
 }
 
 tfk_status tfk_swiglu(const tfk_bf16* gate_up, int64_t in_row_stride, tfk_bf16* out,
@@ -353,6 +439,7 @@ tfk_status tfk_swiglu(const tfk_bf16* gate_up, int64_t in_row_stride, tfk_bf16* 
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: out overlaps gate_up", op);
     tfk_status st;
     if (take_injected(op, &st)) return st;
+    clear_stale_error();
     return finish_launch(op, tfk::launch_swiglu(gate_up, in_row_stride, out, out_row_stride, rows, ffn,
                                                 static_cast<cudaStream_t>(stream)));
 }
@@ -372,6 +459,7 @@ tfk_status tfk_valid_gather(const tfk_bf16* padded, tfk_bf16* compact, int64_t v
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: compact overlaps padded", op);
     tfk_status st;
     if (take_injected(op, &st)) return st;
+    clear_stale_error();
     return finish_launch(op, tfk::launch_valid_gather(padded, compact, valid_rows * hidden / 8,
                                                       static_cast<cudaStream_t>(stream)));
 }
@@ -392,6 +480,7 @@ tfk_status tfk_zero_tail_merge(const tfk_bf16* compact, tfk_bf16* padded, int64_
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: compact overlaps padded", op);
     tfk_status st;
     if (take_injected(op, &st)) return st;
+    clear_stale_error();
     return finish_launch(op, tfk::launch_zero_tail_merge(compact, padded, valid_rows * hidden / 8,
                                                          padded_rows * hidden / 8,
                                                          static_cast<cudaStream_t>(stream)));

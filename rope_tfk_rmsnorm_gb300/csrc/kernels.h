@@ -44,12 +44,20 @@ struct QkRopeArgs {
     const int32_t* pos;
     int64_t rows;         // rows computed from q, k
     int64_t padded_rows;  // rows [rows, padded_rows) of q_out, k_out are written +0.0
+    int heads_per_group;  // output head h goes to group h / heads_per_group (n_heads: one group)
+    int64_t group_stride; // elements between output groups (Ulysses send layout), 0 for one group
     int n_heads;
     int head_dim;
     float theta;
     float eps;
 };
 cudaError_t launch_qk_rmsnorm_rope(const QkRopeArgs& a, cudaStream_t stream);
+
+// Head <-> sequence relayout around the Ulysses all-to-all: pack copies
+// [rows, stride] (n_heads heads of head_dim) into [groups][rows][n_heads/groups][head_dim];
+// unpack is the inverse.
+cudaError_t launch_ulysses_relayout(const uint16_t* src, uint16_t* dst, int64_t row_stride, int64_t rows,
+                                   int n_heads, int head_dim, int groups, bool pack, cudaStream_t stream);
 
 cudaError_t launch_swiglu(const uint16_t* gate_up, int64_t in_stride, uint16_t* out,
                           int64_t out_stride, int64_t rows, int ffn, cudaStream_t stream);

@@ -19,6 +19,9 @@
 // - cos/sin of the D/2 angles of a token are computed once per CTA per token
 //   into a double-buffered shared table (the next token's table is built
 //   while the current token is finished), one barrier per token.
+// - The output can go straight into the Ulysses all-to-all send layout
+//   [groups][rows][heads/groups][D] ("Fuse Q/K RMSNorm, RoPE, and Ulysses
+//   packing", TeleFuser PR #38 section 2): only the store address changes.
 // - Angles are reduced exactly in integer arithmetic: theta^(-2i/D)/(2 pi) is
 //   held as a 64-bit fixed-point fraction of a turn F_i (computed once per
 //   CTA in fp64), pos * F_i mod 2^64 is the angle's fraction of a turn, and
@@ -88,7 +91,10 @@ __global__ void __launch_bounds__(kMaxThreads) qk_rope_kernel(const QkRopeArgs a
         const int h = is_q ? slot[j] : slot[j] - a.n_heads;
         const int64_t col = (int64_t)h * D + lane * 8;
         src0[j] = (is_q ? a.q : a.k) + col;
-        dst0[j] = (is_q ? a.q_out : a.k_out) + col;
+        // output head h: group h / hpg at group_stride, head h % hpg inside the group's row
+        const int grp = h / a.heads_per_group;
+        dst0[j] = (is_q ? a.q_out : a.k_out) + (int64_t)grp * a.group_stride +
+                  (int64_t)(h - grp * a.heads_per_group) * D + lane * 8;
         const float* wsrc = is_q ? a.q_weight : a.k_weight;
         if (active[j]) {
             const float4 x0 = ld_f4(wsrc + lane * 8), x1 = ld_f4(wsrc + lane * 8 + 4);

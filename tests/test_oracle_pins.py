@@ -385,3 +385,27 @@ def test_workload_recipes():
     # a subset of rows is the same rows of the full tensor
     full = synth.activation(t, "gate_up")
     assert np.array_equal(synth.activation(t, "gate_up", rows=[3, 4, 200, 319]), full[[3, 4, 200, 319]])
+
+
+# ---------------------------------------------------------------------------
+# Ulysses relayout
+# ---------------------------------------------------------------------------
+
+def test_ulysses_pack_feeds_an_all_to_all_that_shards_heads():
+    # P ranks each hold T tokens of all H heads; after pack on every rank and the
+    # all-to-all (rank p receives block p from every rank, in rank order), rank p
+    # must hold heads [p*H/P, (p+1)*H/P) of all P*T tokens in sequence order.
+    P, T, H, D = 4, 5, 8, 16
+    glob = np.random.default_rng(0).integers(0, 65536, (P * T, H * D)).astype(np.uint16)
+    sent = [oracle.ulysses_pack(glob[s * T:(s + 1) * T], H, D, P) for s in range(P)]
+    for p in range(P):
+        received = np.concatenate([sent[s][p] for s in range(P)])          # [P*T, H/P, D]
+        expect = glob.reshape(P * T, H, D)[:, p * H // P:(p + 1) * H // P, :]
+        assert np.array_equal(received, expect)
+
+
+def test_ulysses_degree_one_is_identity_and_unpack_inverts_pack():
+    x = np.random.default_rng(1).integers(0, 65536, (7, 6 * 32)).astype(np.uint16)
+    assert np.array_equal(oracle.ulysses_pack(x, 6, 32, 1).reshape(7, -1), x)
+    for P in (1, 2, 3, 6):
+        assert np.array_equal(oracle.ulysses_unpack(oracle.ulysses_pack(x, 6, 32, P), 6, 32, P), x)

@@ -538,3 +538,42 @@ def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
                     wl.head_dim, wl.theta, wl.eps)
     check_close(qo[sample], rq, "valid-only fixed-valid q")
     check_close(ko[sample], rk, "valid-only fixed-valid k")
+
+
+# ---------------------------------------------------------------------------
+# Ulysses: packing fused into Q/K norm + RoPE, and the standalone relayout
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,H,D,P", [(50, 8, 128, 1), (50, 8, 128, 2), (129, 24, 128, 4), (33, 40, 128, 8),
+                                        (17, 6, 64, 3)])
+def test_qk_ulysses_send_layout(cuda, rows, H, D, P):
+    rng = np.random.default_rng(rows + 100 * P)
+    q = rand_bits(rng, (rows, H * D))
+    k = rand_bits(rng, (rows, H * D), 2.0)
+    wq = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    pos = rng.integers(0, 75600, rows).astype(np.int32)
+    qs, ks = tfk.tfk_qk_rmsnorm_rope_neox_ulysses(to_dev(q), to_dev(k), f32_dev(wq), f32_dev(wk), i32_dev(pos),
+                                                  H, D, P)
+    torch.cuda.synchronize()
+    rq, rk = ora_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6)
+    check_close(to_host(qs).reshape(-1), oracle.ulysses_pack(rq, H, D, P).reshape(-1), f"ulysses q P={P}")
+    check_close(to_host(ks).reshape(-1), oracle.ulysses_pack(rk, H, D, P).reshape(-1), f"ulysses k P={P}")
+
+
+@pytest.mark.parametrize("rows,H,D,P,stride_pad", [(1, 1, 8, 1, 0), (100, 24, 128, 4, 0), (77, 40, 128, 8, 64),
+                                                   (5, 6, 40, 3, 8)])
+def test_ulysses_pack_unpack_bit_exact(cuda, rows, H, D, P, stride_pad):
+    rng = np.random.default_rng(rows * H + P)
+    x = rng.integers(0, 65536, (rows, H * D), dtype=np.uint32).astype(np.uint16)
+    src = Guarded(rows, H * D, H * D + stride_pad)
+    src.view.copy_(to_dev(x))
+    packed = tfk.tfk_ulysses_pack(src.view, H, D, P)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(packed), oracle.ulysses_pack(x, H, D, P))
+    back = Guarded(rows, H * D, H * D + stride_pad)
+    tfk.tfk_ulysses_unpack(packed, H, D, P, dst=back.view)
+    torch.cuda.synchronize()
+    back.check()
+    src.check()
+    assert np.array_equal(back.host(), x)
