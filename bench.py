@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-valid-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every kernel on every workload (one JSON line per workload) instead of the step")
     return ap.parse_args(argv)
 
 
@@ -552,10 +554,86 @@ def run_tfk(args, ranks: Ranks) -> dict | None:
             "valid_only": valid, "cpu_baseline": cpu}
 
 
+class Single:
+    """One kernel of a workload as a timed unit (the per-kernel sweep)."""
+
+    def __init__(self, name, nbytes, fn):
+        self.kernels, self.bytes, self.fn = [name], [nbytes], fn
+
+    def launch(self, ev=None):
+        if ev:
+            ev[0].record()
+        self.fn()
+        if ev:
+            ev[1].record()
+
+
+def run_sweep(args, ranks: Ranks):
+    """Every kernel on every workload at full size; one JSON line per workload (rank 0)."""
+    import rope_tfk_rmsnorm_gb300 as tfk
+    tfk.load()
+    device = torch.device("cuda", ranks.local_rank)
+    torch.cuda.set_device(device)
+    peak = measured_peaks()["hbm_gbs"]
+    K, W = max(1, min(args.steps, 100)), max(3, args.warmup)
+    for name in ("tiny", "medium", "valid_only", "large", "per_frame"):
+        wl = synth.get(name)
+        res = {}
+        if name == "valid_only":
+            vo = ValidOnly(tfk, wl, device)
+            L, N, hd = vo.L, vo.N, wl.hidden
+            fx = lambda: tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(  # noqa: E731
+                vo.pad["x"], L, vo.params["w"], vo.params["shift"], vo.params["scale"], vo.idx, wl.eps,
+                out=vo.merged["y"])
+            fq = lambda: tfk.tfk_qk_rmsnorm_rope_neox_fixed_valid(  # noqa: E731
+                vo.pad["q"], vo.pad["k"], L, vo.params["w_q"], vo.params["w_k"], vo.pos, wl.n_heads, wl.head_dim,
+                wl.theta, wl.eps, q_out=vo.merged["q"], k_out=vo.merged["k"])
+            units = [
+                Single("valid_gather", bytes_gather(L, hd), lambda: tfk.tfk_valid_gather(vo.pad["x"], L, compact=vo.comp["x"])),
+                Single("zero_tail_merge", bytes_merge(L, N, hd), lambda: tfk.tfk_zero_tail_merge(vo.res["y"], vo.merged["y"])),
+                Single("rmsnorm_adaln_fixed_valid", bytes_adaln(L, hd, 2) + 2 * hd * (N - L), fx),
+                Single("qk_rmsnorm_rope_fixed_valid", bytes_qk(L, wl.n_heads, wl.head_dim) + 4 * hd * (N - L), fq),
+                vo,
+            ]
+            rows_for = {"valid_gather": L, "zero_tail_merge": L, "rmsnorm_adaln_fixed_valid": L,
+                        "qk_rmsnorm_rope_fixed_valid": L}
+        else:
+            ch = Chain(tfk, wl, device)
+            units = [Single(n, b, f) for n, b, f in zip(
+                ch.kernels, ch.bytes,
+                [lambda: tfk.tfk_rmsnorm_adaln_indexed(ch.d["x"], ch.params["w"], ch.params["shift"],
+                                                       ch.params["scale"], ch.d["idx"], wl.eps, out=ch.out["y"]),
+                 lambda: tfk.tfk_qk_rmsnorm_rope_neox(ch.d["q"], ch.d["k"], ch.params["w_q"], ch.params["w_k"],
+                                                      ch.d["pos"], wl.n_heads, wl.head_dim, wl.theta, wl.eps,
+                                                      q_out=ch.out["q"], k_out=ch.out["k"]),
+                 lambda: tfk.tfk_swiglu(ch.d["gate_up"], out=ch.out["o"])])] + [ch]
+            rows_for = {}
+        for u in units:
+            total, per, _, _ = time_steps(u, K, W, ranks)
+            if len(u.kernels) == 1:
+                ms = per[0]
+                rows = rows_for.get(u.kernels[0], wl.rows)
+                res[u.kernels[0]] = dict(_roof(u.bytes[0], ms, peak), tokens_per_s=rows / (ms * 1e-3))
+            else:
+                ms = total / K
+                rows = vo.L if name == "valid_only" else wl.rows
+                res["chain" if name != "valid_only" else "valid_only_pipeline"] = dict(
+                    _roof(sum(u.bytes), ms, peak), tokens_per_s=rows / (ms * 1e-3),
+                    kernels=u.kernels)
+        if ranks.rank == 0:
+            print(json.dumps({"sweep": name, "workload": workload_config(wl)["workload"], "steps": K,
+                              "peak_gbs": peak, "results": res}), flush=True)
+        del units
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     ranks = Ranks()
     try:
+        if args.sweep:
+            run_sweep(args, ranks)
+            return
         out = run_reference(args, ranks) if args.impl == "reference" else run_tfk(args, ranks)
         if out is not None:
             print(json.dumps(out), flush=True)

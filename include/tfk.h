@@ -110,9 +110,7 @@ tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride,
  *               (q_out == q and k_out == k with equal strides) is allowed.
  * q_weight, k_weight  [head_dim] fp32, shared by every head.
  * positions     [rows] int32 token positions (any int32 value).
- * head_dim      multiple of 16, 16 <= head_dim <= 512; n_heads >= 1 and
- *               2 * n_heads * G <= 2048, G = head_dim/16 rounded up to a power
- *               of two (n_heads <= 128 at head_dim 128).
+ * head_dim      multiple of 16, 16 <= head_dim <= 512; 1 <= n_heads <= 2^20.
  * theta > 0 (RoPE base, 10000 in the usual setting); eps >= 0.
  * The angle is reduced modulo one turn exactly enough that positions up to
  * 2^31 keep full fp32 accuracy in cos/sin.

@@ -276,7 +276,7 @@ tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: theta must be finite and > 0", op);
     if (head_dim % 16 != 0 || !tfk::qk_rope_supported(n_heads, head_dim))
         return fail(TFK_ERR_UNSUPPORTED, "%s: head_dim = %d, n_heads = %d not supported (head_dim a multiple "
-                    "of 16 in [16, 512]; 2*n_heads*pow2(head_dim/16) <= 2048)", op, head_dim, n_heads);
+                    "of 16 in [16, 512], n_heads <= 2^20)", op, head_dim, n_heads);
     if (sp_degree < 0 || (sp_degree > 0 && n_heads % sp_degree != 0))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: sp_degree %d must divide n_heads %d", op, sp_degree, n_heads);
     const int64_t width = (int64_t)n_heads * head_dim;

@@ -9,254 +9,267 @@
 // "Q/K normalization plus NeoX RoPE", TeleFuser PR #23 "Changes Made").
 //
 // Design (HBM-bound: 4 bytes per q/k element read + written, plus 4 B/token):
-// - Persistent CTAs over contiguous token runs.  A head is served by G lanes
-//   (G = D/16 rounded up to a power of two); lane l holds the 8-element
-//   vector l of the first half and vector l of the second half, so every
-//   rotate-half pair sits in one thread and needs no shuffle.  The per-head
-//   sum of squares is a G-lane shuffle reduction.
-// - q/k head rows are staged through a shared-memory ring with cp.async,
-//   stages-1 tokens ahead; each thread reads back only its own slots.
-// - cos/sin of the D/2 angles of a token are computed once per CTA per token
-//   into a double-buffered shared table (the next token's table is built
-//   while the current token is finished), one barrier per token.
-// - The output can go straight into the Ulysses all-to-all send layout
-//   [groups][rows][heads/groups][D] ("Fuse Q/K RMSNorm, RoPE, and Ulysses
-//   packing", TeleFuser PR #38 section 2): only the store address changes.
+// - A head is served by G lanes (G = D/16 rounded up to a power of two);
+//   lane l holds the 8-element vector l of the first half and vector l of the
+//   second half, so every rotate-half pair sits in one thread and needs no
+//   shuffle; the per-head sum of squares is a G-lane shuffle reduction.
+// - A group of G lanes owns HPT heads of the same tensor (q or k), so its
+//   weights stay in registers and the 8 cos/sin values a lane needs for a
+//   token are computed once and used for HPT heads.  Nothing is shared across
+//   warps: there is no barrier anywhere in the token loop.
+// - The grid is 2-D: contiguous token runs x chunks of head groups (any head
+//   count fits), persistent over the token runs.  Each thread streams its own
+//   head vectors through a shared-memory ring with cp.async, stages-1 tokens
+//   ahead, and reads back only the slots it copied itself.
 // - Angles are reduced exactly in integer arithmetic: theta^(-2i/D)/(2 pi) is
 //   held as a 64-bit fixed-point fraction of a turn F_i (computed once per
 //   CTA in fp64), pos * F_i mod 2^64 is the angle's fraction of a turn, and
-//   its top 32 bits give an fp32 angle in [-pi, pi) for sincosf.  The error
-//   of the reduced angle is below 2^-40 turn for any int32 position, so no
-//   fp64 work is needed per token (fp64 throughput on GB300 is low).
+//   its top 32 bits give an fp32 angle in [-pi, pi).  On that range the
+//   hardware sin/cos approximations are accurate to about 4e-7 absolute, so
+//   no fp64 and no range reduction is needed per token.
+// - The output can go straight into the Ulysses all-to-all send layout
+//   [groups][rows][heads/groups][D] ("Fuse Q/K RMSNorm, RoPE, and Ulysses
+//   packing", TeleFuser PR #38 section 2): only the store address changes.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace tfk {
 namespace {
 
-constexpr int kMaxThreads = 512;
+// 160 threads = 20 lane groups of 8 (head_dim 128): all 80 q/k heads of a
+// 40-head token in one CTA at 4 heads per group; at most 102 registers so
+// that four CTAs share an SM.
+constexpr int kMaxThreads = 160;
+constexpr int kMinBlocks = 4;
 
-__device__ __forceinline__ float2 rope_cos_sin(int32_t pos, uint64_t turn_fraction) {
+__device__ __forceinline__ void rope_cos_sin(int32_t pos, uint64_t turn_fraction, float& c, float& s) {
     const uint64_t a = (uint64_t)(int64_t)pos * turn_fraction;        // mod 2^64 = mod one turn
     const int32_t top = (int32_t)(uint32_t)(a >> 32);                   // [-2^31, 2^31) -> [-pi, pi)
     const float angle = (float)top * 1.46291807926715968e-9f;           // 2 pi / 2^32
-    float s, c;
-    sincosf(angle, &s, &c);
-    return make_float2(c, s);
+    __sincosf(angle, &s, &c);
 }
 
+struct Layout {
+    int hpt;          // heads per lane group (all of one tensor)
+    int lanes;        // G
+    int threads;      // per CTA
+    int groups;       // lane groups in the whole problem: 2 * n_heads / hpt
+    int head_chunks;  // CTAs along the head dimension
+};
+
 template <int HPT>
-__global__ void __launch_bounds__(kMaxThreads) qk_rope_kernel(const QkRopeArgs a, const int lanes_per_head,
-                                                              const int stages) {
+__global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const QkRopeArgs a, const Layout lay,
+                                                              const int token_chunks, const int stages) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int nt = blockDim.x;
     const int tid = threadIdx.x;
     const int D = a.head_dim;
     const int half = D >> 1;
     const int L = D >> 4;                 // lanes holding data per head
-    const int G = lanes_per_head;         // power of two >= L
-    const int slots = 2 * a.n_heads;      // q heads then k heads
-    const int heads_per_pass = nt / G;
+    const int G = lay.lanes;
     const float inv_d = 1.0f / (float)D;
 
     Vec8* ring = reinterpret_cast<Vec8*>(smem_raw);                   // [stages][HPT][2][nt]
     const int stage_vecs = HPT * 2 * nt;
     uint64_t* ftab = reinterpret_cast<uint64_t*>(ring + (int64_t)stages * stage_vecs);  // [half]
-    float2* cs = reinterpret_cast<float2*>(ftab + half);              // [2][half]
 
-    const int64_t r0 = a.rows * (int64_t)blockIdx.x / gridDim.x;
-    const int64_t r1 = a.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
+    const int tchunk = blockIdx.x % token_chunks;
+    const int hchunk = blockIdx.x / token_chunks;
+    const int64_t r0 = a.rows * (int64_t)tchunk / token_chunks;
+    const int64_t r1 = a.rows * (int64_t)(tchunk + 1) / token_chunks;
     const int nrows = (int)(r1 - r0);
 
-    // Fixed-point turn fractions of the D/2 frequencies.  Thread tid owns the
-    // entries i = tid (mod nt) and is the only one to read them back.
+    // fixed-point turn fractions of the D/2 frequencies, shared by the CTA
     for (int i = tid; i < half; i += nt) {
         const double f = pow((double)a.theta, -2.0 * (double)i / (double)D);
         double turns = f * 0.15915494309189533577;  // 1 / (2 pi)
         turns -= floor(turns);
         ftab[i] = __double2ull_rz(turns * 18446744073709551616.0);  // * 2^64
     }
+    __syncthreads();
 
     const int lane = tid % G;
-    int slot[HPT];
-    bool active[HPT];
-    const uint16_t* src0[HPT];
-    uint16_t* dst0[HPT];
-    float wa[HPT][8], wb[HPT][8];
+    const int group = hchunk * (nt / G) + tid / G;
+    const bool active = group < lay.groups && lane < L;
+    const int slot0 = group * HPT;                  // first head slot: q heads, then k heads
+    const bool is_q = slot0 < a.n_heads;
+    const int h0 = is_q ? slot0 : slot0 - a.n_heads;
+    const uint16_t* src0 = (is_q ? a.q : a.k) + (int64_t)h0 * D + lane * 8;
+    uint16_t* outp = is_q ? a.q_out : a.k_out;
+    const float* wsrc = is_q ? a.q_weight : a.k_weight;
+    float wa[8], wb[8];
+    const uint64_t* fq = ftab + (active ? lane * 8 : 0);  // this lane's 8 frequencies, read per token
+    if (active) {
+        const float4 x0 = ld_f4(wsrc + lane * 8), x1 = ld_f4(wsrc + lane * 8 + 4);
+        const float4 y0 = ld_f4(wsrc + half + lane * 8), y1 = ld_f4(wsrc + half + lane * 8 + 4);
+        wa[0] = x0.x; wa[1] = x0.y; wa[2] = x0.z; wa[3] = x0.w; wa[4] = x1.x; wa[5] = x1.y; wa[6] = x1.z; wa[7] = x1.w;
+        wb[0] = y0.x; wb[1] = y0.y; wb[2] = y0.z; wb[3] = y0.w; wb[4] = y1.x; wb[5] = y1.y; wb[6] = y1.z; wb[7] = y1.w;
+    } else {
 #pragma unroll
-    for (int j = 0; j < HPT; ++j) {
-        slot[j] = tid / G + j * heads_per_pass;
-        active[j] = slot[j] < slots && lane < L;
-        const bool is_q = slot[j] < a.n_heads;
-        const int h = is_q ? slot[j] : slot[j] - a.n_heads;
-        const int64_t col = (int64_t)h * D + lane * 8;
-        src0[j] = (is_q ? a.q : a.k) + col;
-        // output head h: group h / hpg at group_stride, head h % hpg inside the group's row
-        const int grp = h / a.heads_per_group;
-        dst0[j] = (is_q ? a.q_out : a.k_out) + (int64_t)grp * a.group_stride +
-                  (int64_t)(h - grp * a.heads_per_group) * D + lane * 8;
-        const float* wsrc = is_q ? a.q_weight : a.k_weight;
-        if (active[j]) {
-            const float4 x0 = ld_f4(wsrc + lane * 8), x1 = ld_f4(wsrc + lane * 8 + 4);
-            const float4 y0 = ld_f4(wsrc + half + lane * 8), y1 = ld_f4(wsrc + half + lane * 8 + 4);
-            wa[j][0] = x0.x; wa[j][1] = x0.y; wa[j][2] = x0.z; wa[j][3] = x0.w;
-            wa[j][4] = x1.x; wa[j][5] = x1.y; wa[j][6] = x1.z; wa[j][7] = x1.w;
-            wb[j][0] = y0.x; wb[j][1] = y0.y; wb[j][2] = y0.z; wb[j][3] = y0.w;
-            wb[j][4] = y1.x; wb[j][5] = y1.y; wb[j][6] = y1.z; wb[j][7] = y1.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { wa[j][e] = 0.f; wb[j][e] = 0.f; }
-        }
+        for (int e = 0; e < 8; ++e) { wa[e] = 0.f; wb[e] = 0.f; }
     }
+    // output address of head slot j: group h / hpg at group_stride, head h % hpg inside it
+    auto out_base = [&](int j) -> uint16_t* {
+        const int h = h0 + j;
+        const int grp = h / a.heads_per_group;
+        return outp + (int64_t)grp * a.group_stride + (int64_t)(h - grp * a.heads_per_group) * D + lane * 8;
+    };
 
     auto issue = [&](int row_in_run, int stage) {
-        const int64_t roff_in = (r0 + row_in_run) * a.in_stride;
-        Vec8* st = ring + (int64_t)stage * stage_vecs;
+        const uint16_t* src = src0 + (r0 + row_in_run) * a.in_stride;
+        Vec8* st = ring + (int64_t)stage * stage_vecs + tid;
 #pragma unroll
         for (int j = 0; j < HPT; ++j) {
-            if (active[j]) {
-                cp_async16(st + (j * 2 + 0) * nt + tid, src0[j] + roff_in);
-                cp_async16(st + (j * 2 + 1) * nt + tid, src0[j] + roff_in + half);
-            }
+            cp_async16(st + (j * 2 + 0) * nt, src + j * D);
+            cp_async16(st + (j * 2 + 1) * nt, src + j * D + half);
         }
     };
 
     if (nrows > 0) {  // uniform over the CTA
-    for (int s = 0; s < stages - 1; ++s) {
-        if (s < nrows) issue(s, s);
-        cp_async_commit();
-    }
-    {   // cos/sin table of the first token
-        const int32_t p = __ldg(a.pos + r0);
-        for (int i = tid; i < half; i += nt) cs[i] = rope_cos_sin(p, ftab[i]);
-    }
+        for (int s = 0; s < stages - 1; ++s) {
+            if (active && s < nrows) issue(s, s);
+            cp_async_commit();
+        }
+        int stage_rd = 0, stage_wr = stages - 1;
+        int32_t p_next = __ldg(a.pos + r0);
+        for (int it = 0; it < nrows; ++it) {
+            const int64_t r = r0 + it;
+            const int ahead = it + stages - 1;
+            if (active && ahead < nrows) issue(ahead, stage_wr);
+            cp_async_commit();
+            stage_wr = stage_wr + 1 == stages ? 0 : stage_wr + 1;
+            const int32_t p = p_next;
+            if (it + 1 < nrows) p_next = __ldg(a.pos + r + 1);
 
-    for (int it = 0; it < nrows; ++it) {
-        const int64_t r = r0 + it;
-        const int ahead = it + stages - 1;
-        if (ahead < nrows) issue(ahead, ahead % stages);
-        cp_async_commit();
-        cp_async_wait_dyn(stages - 1);
-        __syncthreads();  // publishes cs[it & 1]
-
-        const Vec8* st = ring + (int64_t)(it % stages) * stage_vecs;
-        const float2* tab = cs + (it & 1) * half + lane * 8;
+            float cs[8], sn[8];
 #pragma unroll
-        for (int j = 0; j < HPT; ++j) {
-            float va[8], vb[8];
-            float ss = 0.f;
-            if (active[j]) {
-                unpack8(ld_smem_vec(st + (j * 2 + 0) * nt + tid), va);
-                unpack8(ld_smem_vec(st + (j * 2 + 1) * nt + tid), vb);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(va[e], va[e], fmaf(vb[e], vb[e], ss));
+            for (int e = 0; e < 8; e += 2) {
+                const ulonglong2 f2 = *reinterpret_cast<const ulonglong2*>(fq + e);
+                rope_cos_sin(p, f2.x, cs[e], sn[e]);
+                rope_cos_sin(p, f2.y, cs[e + 1], sn[e + 1]);
             }
-            for (int o = G >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-            if (active[j]) {
-                const float inv_rms = rsqrtf(ss * inv_d + a.eps);
-                float oa[8], ob[8];
+
+            cp_async_wait_dyn(stages - 1);
+            const Vec8* st = ring + (int64_t)stage_rd * stage_vecs + tid;
+            stage_rd = stage_rd + 1 == stages ? 0 : stage_rd + 1;
+
+            float ss[HPT];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 c = tab[e];
-                    const float na = va[e] * inv_rms * wa[j][e];
-                    const float nb = vb[e] * inv_rms * wb[j][e];
-                    oa[e] = fmaf(na, c.x, -nb * c.y);
-                    ob[e] = fmaf(nb, c.x, na * c.y);
-                }
+            for (int j = 0; j < HPT; ++j) {
+                float va[8], vb[8];
+                unpack8(ld_smem_vec(st + (j * 2 + 0) * nt), va);
+                unpack8(ld_smem_vec(st + (j * 2 + 1) * nt), vb);
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { s0 = fmaf(va[e], va[e], s0); s1 = fmaf(vb[e], vb[e], s1); }
+                ss[j] = active ? s0 + s1 : 0.f;
+            }
+            for (int o = G >> 1; o > 0; o >>= 1) {
+#pragma unroll
+                for (int j = 0; j < HPT; ++j) ss[j] += __shfl_xor_sync(0xFFFFFFFFu, ss[j], o);
+            }
+            if (active) {
                 const int64_t roff = r * a.out_stride;
-                st_vec(dst0[j] + roff, pack8(oa));
-                st_vec(dst0[j] + roff + half, pack8(ob));
+#pragma unroll
+                for (int j = 0; j < HPT; ++j) {
+                    float va[8], vb[8], oa[8], ob[8];
+                    unpack8(ld_smem_vec(st + (j * 2 + 0) * nt), va);
+                    unpack8(ld_smem_vec(st + (j * 2 + 1) * nt), vb);
+                    const float inv_rms = rsqrtf(ss[j] * inv_d + a.eps);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float na = va[e] * inv_rms * wa[e];
+                        const float nb = vb[e] * inv_rms * wb[e];
+                        oa[e] = fmaf(na, cs[e], -nb * sn[e]);
+                        ob[e] = fmaf(nb, cs[e], na * sn[e]);
+                    }
+                    uint16_t* o = out_base(j) + roff;
+                    st_vec(o, pack8(oa));
+                    st_vec(o + half, pack8(ob));
+                }
             }
         }
-
-        if (it + 1 < nrows) {  // next token's table, into the other buffer
-            const int32_t p = __ldg(a.pos + r + 1);
-            float2* nxt = cs + ((it + 1) & 1) * half;
-            for (int i = tid; i < half; i += nt) nxt[i] = rope_cos_sin(p, ftab[i]);
-        }
-    }
-    cp_async_wait<0>();
+        cp_async_wait<0>();
     }  // nrows > 0
 
     // Fixed-valid mode: this CTA's share of the padded tail rows of q_out and
     // k_out is written +0.0 in the same launch (the input tail is never read).
     const int64_t tail = a.padded_rows - a.rows;
-    if (tail > 0) {
-        const int64_t z0 = a.rows + tail * (int64_t)blockIdx.x / gridDim.x;
-        const int64_t z1 = a.rows + tail * (int64_t)(blockIdx.x + 1) / gridDim.x;
+    if (tail > 0 && active) {
+        const int64_t z0 = a.rows + tail * (int64_t)tchunk / token_chunks;
+        const int64_t z1 = a.rows + tail * (int64_t)(tchunk + 1) / token_chunks;
         Vec8 zero;
         zero.w[0] = zero.w[1] = zero.w[2] = zero.w[3] = 0u;
         for (int64_t r = z0; r < z1; ++r) {
             const int64_t roff = r * a.out_stride;
 #pragma unroll
             for (int j = 0; j < HPT; ++j) {
-                if (active[j]) {
-                    st_vec(dst0[j] + roff, zero);
-                    st_vec(dst0[j] + roff + half, zero);
-                }
+                uint16_t* o = out_base(j) + roff;
+                st_vec(o, zero);
+                st_vec(o + half, zero);
             }
         }
     }
 }
 
-struct Shape {
-    int hpt, threads, lanes;
-};
-
-bool choose_shape(int n_heads, int head_dim, Shape* s) {
-    if (head_dim < 16 || head_dim > 512 || head_dim % 16 != 0 || n_heads < 1) return false;
+bool choose_layout(int n_heads, int head_dim, Layout* lay) {
+    if (head_dim < 16 || head_dim > 512 || head_dim % 16 != 0 || n_heads < 1 || n_heads > (1 << 20)) return false;
     int L = head_dim / 16, G = 1;
     while (G < L) G <<= 1;
-    const int64_t slots = 2LL * n_heads;
-    for (int hpt = 1; hpt <= 4; hpt *= 2) {
-        const int64_t t = (slots + hpt - 1) / hpt * G;
-        const int64_t threads = (t + 31) / 32 * 32;
-        if (threads <= kMaxThreads) {
-            s->hpt = hpt;
-            s->threads = (int)threads;
-            s->lanes = G;
-            return true;
-        }
-    }
-    return false;
+    int hpt = n_heads % 4 == 0 ? 4 : (n_heads % 2 == 0 ? 2 : 1);
+    const int64_t groups = 2LL * n_heads / hpt;
+    // as few head chunks as possible with at most kMaxThreads threads per CTA
+    const int64_t per_cta = kMaxThreads / G;
+    const int64_t chunks = (groups + per_cta - 1) / per_cta;
+    const int64_t groups_per_cta = (groups + chunks - 1) / chunks;
+    const int64_t threads = (groups_per_cta * G + 31) / 32 * 32;
+    lay->hpt = hpt;
+    lay->lanes = G;
+    lay->threads = (int)threads;
+    lay->groups = (int)groups;
+    lay->head_chunks = (int)chunks;
+    return chunks <= 65535;
 }
 
 template <int HPT>
-cudaError_t launch_h(const QkRopeArgs& a, const Shape& s, cudaStream_t stream) {
+cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
-    const int stage_bytes = HPT * 2 * s.threads * 16;
-    const int table_bytes = (a.head_dim / 2) * (8 + 2 * 8);
+    const int stage_bytes = HPT * 2 * lay.threads * 16;
+    const int table_bytes = (a.head_dim / 2) * 8;
     const void* fn = reinterpret_cast<const void*>(&qk_rope_kernel<HPT>);
-    const int by_regs = blocks_per_sm(fn, s.threads, table_bytes);
+    const int by_regs = blocks_per_sm(fn, lay.threads, table_bytes + 2 * stage_bytes);
     if (by_regs <= 0) return cudaErrorInvalidConfiguration;
-    const int stages = pick_stages(by_regs >= 2 ? 2 : 1, stage_bytes, table_bytes);
+    const int stages = pick_stages(by_regs, stage_bytes, table_bytes);
     const size_t smem = (size_t)stages * stage_bytes + table_bytes;
-    const int per_sm = blocks_per_sm(fn, s.threads, smem);
+    const int per_sm = blocks_per_sm(fn, lay.threads, smem);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-    int64_t grid = (int64_t)per_sm * di.sm_count;
+    // token runs: enough CTAs for every SM, and no more runs than rows to work on
+    int64_t want = ((int64_t)per_sm * di.sm_count + lay.head_chunks - 1) / lay.head_chunks;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
-    if (grid > work) grid = work;
-    if (grid < 1) return cudaSuccess;
-    qk_rope_kernel<HPT><<<(unsigned)grid, s.threads, smem, stream>>>(a, s.lanes, stages);
+    if (want > work) want = work;
+    if (want < 1) return cudaSuccess;
+    const int64_t grid = want * lay.head_chunks;
+    if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    qk_rope_kernel<HPT><<<(unsigned)grid, lay.threads, smem, stream>>>(a, lay, (int)want, stages);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool qk_rope_supported(int n_heads, int head_dim) {
-    Shape s;
-    return choose_shape(n_heads, head_dim, &s);
+    Layout lay;
+    return choose_layout(n_heads, head_dim, &lay);
 }
 
 cudaError_t launch_qk_rmsnorm_rope(const QkRopeArgs& a, cudaStream_t stream) {
-    Shape s;
-    if (!choose_shape(a.n_heads, a.head_dim, &s)) return cudaErrorInvalidValue;
-    switch (s.hpt) {
-        case 1: return launch_h<1>(a, s, stream);
-        case 2: return launch_h<2>(a, s, stream);
-        default: return launch_h<4>(a, s, stream);
+    Layout lay;
+    if (!choose_layout(a.n_heads, a.head_dim, &lay)) return cudaErrorInvalidValue;
+    switch (lay.hpt) {
+        case 1: return launch_h<1>(a, lay, stream);
+        case 2: return launch_h<2>(a, lay, stream);
+        default: return launch_h<4>(a, lay, stream);
     }
 }
 

@@ -26,11 +26,15 @@ namespace tfk {
 namespace {
 
 constexpr int kMaxThreads = 512;
+constexpr int kMaxThreadsV1 = 384;
 
+// Combined modulation of the columns a thread owns for modulation row m:
+//   mul = w * (1 + scale[m]),  add = shift[m]
+// so that y = x * inv_rms * mul + add (one fp32 rounding of w * (1 + scale)
+// more than the literal formula; far below the bf16 rounding of y).
 template <int V>
 __device__ __forceinline__ void load_mod_row(const AdalnArgs& a, int m, const int (&col)[V],
-                                             const bool (&ok)[V], float (&sh)[V][8],
-                                             float (&sc)[V][8]) {
+                                             const bool (&ok)[V], float (&mul)[V][8], float (&add)[V][8]) {
     const float* srow = a.shift + (int64_t)m * a.hidden;
     const float* crow = a.scale + (int64_t)m * a.hidden;
 #pragma unroll
@@ -38,16 +42,27 @@ __device__ __forceinline__ void load_mod_row(const AdalnArgs& a, int m, const in
         if (ok[i]) {
             const float4 s0 = ld_f4(srow + col[i] * 8), s1 = ld_f4(srow + col[i] * 8 + 4);
             const float4 c0 = ld_f4(crow + col[i] * 8), c1 = ld_f4(crow + col[i] * 8 + 4);
-            sh[i][0] = s0.x; sh[i][1] = s0.y; sh[i][2] = s0.z; sh[i][3] = s0.w;
-            sh[i][4] = s1.x; sh[i][5] = s1.y; sh[i][6] = s1.z; sh[i][7] = s1.w;
-            sc[i][0] = 1.0f + c0.x; sc[i][1] = 1.0f + c0.y; sc[i][2] = 1.0f + c0.z; sc[i][3] = 1.0f + c0.w;
-            sc[i][4] = 1.0f + c1.x; sc[i][5] = 1.0f + c1.y; sc[i][6] = 1.0f + c1.z; sc[i][7] = 1.0f + c1.w;
+            const float4 w0 = ld_f4(a.weight + col[i] * 8), w1 = ld_f4(a.weight + col[i] * 8 + 4);
+            add[i][0] = s0.x; add[i][1] = s0.y; add[i][2] = s0.z; add[i][3] = s0.w;
+            add[i][4] = s1.x; add[i][5] = s1.y; add[i][6] = s1.z; add[i][7] = s1.w;
+            mul[i][0] = w0.x * (1.0f + c0.x); mul[i][1] = w0.y * (1.0f + c0.y);
+            mul[i][2] = w0.z * (1.0f + c0.z); mul[i][3] = w0.w * (1.0f + c0.w);
+            mul[i][4] = w1.x * (1.0f + c1.x); mul[i][5] = w1.y * (1.0f + c1.y);
+            mul[i][6] = w1.z * (1.0f + c1.z); mul[i][7] = w1.w * (1.0f + c1.w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { mul[i][e] = 0.f; add[i][e] = 0.f; }
         }
     }
 }
 
+// One or two vectors per thread (hidden <= 8192) run at least two CTAs per
+// SM, so that their per-row reductions and barriers overlap: one vector per
+// thread (at most 384 threads, two cached modulation rows) within 85
+// registers, two vectors within 64; wider rows get the full register file.
 template <int V>
-__global__ void __launch_bounds__(kMaxThreads) rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
+__global__ void __launch_bounds__(V == 1 ? kMaxThreadsV1 : kMaxThreads, V <= 2 ? 2 : 1)
+rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Vec8* ring = reinterpret_cast<Vec8*>(smem_raw);  // [stages][nvec]
     __shared__ float partial[2][32];
@@ -66,119 +81,110 @@ __global__ void __launch_bounds__(kMaxThreads) rmsnorm_adaln_kernel(const AdalnA
 
     int col[V];
     bool ok[V];
-    float w[V][8];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
         col[i] = tid + i * nt;
         ok[i] = col[i] < nvec;
-        if (ok[i]) {
-            const float4 w0 = ld_f4(a.weight + col[i] * 8), w1 = ld_f4(a.weight + col[i] * 8 + 4);
-            w[i][0] = w0.x; w[i][1] = w0.y; w[i][2] = w0.z; w[i][3] = w0.w;
-            w[i][4] = w1.x; w[i][5] = w1.y; w[i][6] = w1.z; w[i][7] = w1.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[i][e] = 0.f;
-        }
     }
 
     if (nrows > 0) {  // uniform over the CTA
-    // Prologue: rows 0 .. stages-2 of this CTA's run go in flight.
-    for (int s = 0; s < stages - 1; ++s) {
-        if (s < nrows) {
-            const uint16_t* src = a.x + (r0 + s) * a.x_stride;
-            Vec8* dst = ring + (int64_t)s * nvec;
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-                if (ok[i]) cp_async16(dst + col[i], src + col[i] * 8);
-        }
-        cp_async_commit();
-    }
-
-    float sh[V][8], sc[V][8];
-    float sh2[V == 1 ? V : 1][8], sc2[V == 1 ? V : 1][8];
-    int m_cur = -1, m_alt = -1;
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { sh[i][e] = 0.f; sc[i][e] = 0.f; }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) { sh2[0][e] = 0.f; sc2[0][e] = 0.f; }
-    int m_next = __ldg(a.mod_idx + r0);
-
-    for (int it = 0; it < nrows; ++it) {
-        const int64_t r = r0 + it;
-        {   // keep stages-1 rows in flight
-            const int ahead = it + stages - 1;
-            if (ahead < nrows) {
-                const uint16_t* src = a.x + (r0 + ahead) * a.x_stride;
-                Vec8* dst = ring + (int64_t)(ahead % stages) * nvec;
+        // Prologue: rows 0 .. stages-2 of this CTA's run go in flight.
+        for (int s = 0; s < stages - 1; ++s) {
+            if (s < nrows) {
+                const uint16_t* src = a.x + (r0 + s) * a.x_stride;
+                Vec8* dst = ring + (int64_t)s * nvec;
 #pragma unroll
                 for (int i = 0; i < V; ++i)
                     if (ok[i]) cp_async16(dst + col[i], src + col[i] * 8);
             }
             cp_async_commit();
         }
-        const int m = m_next;
-        if (it + 1 < nrows) m_next = __ldg(a.mod_idx + r + 1);
-        cp_async_wait_dyn(stages - 1);
 
-        const Vec8* cur = ring + (int64_t)(it % stages) * nvec;
-        float xf[V][8];
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            if (ok[i]) {
-                unpack8(ld_smem_vec(cur + col[i]), xf[i]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xf[i][e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(xf[i][e], xf[i][e], ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) partial[it & 1][warp] = ss;
-        __syncthreads();
-        float total = 0.f;
-        for (int k = 0; k < nwarps; ++k) total += partial[it & 1][k];
-        const float inv_rms = rsqrtf(total * inv_hidden + a.eps);
+        float mul[V][8], add[V][8];
+        float mul2[1][8], add2[1][8];  // second cached row (used when V == 1)
+        int m_cur = -1, m_alt = -1;
+        int m_next = __ldg(a.mod_idx + r0);
+        int stage_rd = 0, stage_wr = stages - 1;
 
-        if (m != m_cur) {  // uniform over the CTA
-            if constexpr (V == 1) {
-                if (m == m_alt) {
+        for (int it = 0; it < nrows; ++it) {
+            const int64_t r = r0 + it;
+            {   // keep stages-1 rows in flight
+                const int ahead = it + stages - 1;
+                if (ahead < nrows) {
+                    const uint16_t* src = a.x + (r0 + ahead) * a.x_stride;
+                    Vec8* dst = ring + (int64_t)stage_wr * nvec;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float ts = sh[0][e], tc = sc[0][e];
-                        sh[0][e] = sh2[0][e]; sc[0][e] = sc2[0][e];
-                        sh2[0][e] = ts; sc2[0][e] = tc;
-                    }
-                    m_alt = m_cur;
-                    m_cur = m;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) { sh2[0][e] = sh[0][e]; sc2[0][e] = sc[0][e]; }
-                    m_alt = m_cur;
-                    load_mod_row<V>(a, m, col, ok, sh, sc);
-                    m_cur = m;
+                    for (int i = 0; i < V; ++i)
+                        if (ok[i]) cp_async16(dst + col[i], src + col[i] * 8);
                 }
-            } else {
-                load_mod_row<V>(a, m, col, ok, sh, sc);
+                cp_async_commit();
+                stage_wr = stage_wr + 1 == stages ? 0 : stage_wr + 1;
+            }
+            const int m = m_next;
+            if (it + 1 < nrows) m_next = __ldg(a.mod_idx + r + 1);
+            cp_async_wait_dyn(stages - 1);
+
+            const Vec8* cur = ring + (int64_t)stage_rd * nvec;
+            stage_rd = stage_rd + 1 == stages ? 0 : stage_rd + 1;
+            Vec8 xv[V];
+            float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                if (ok[i]) {
+                    xv[i] = ld_smem_vec(cur + col[i]);
+                } else {
+                    xv[i].w[0] = xv[i].w[1] = xv[i].w[2] = xv[i].w[3] = 0u;
+                }
+                float f[8];
+                unpack8(xv[i], f);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    ss0 = fmaf(f[e], f[e], ss0);
+                    ss1 = fmaf(f[e + 1], f[e + 1], ss1);
+                }
+            }
+            float ss = warp_sum(ss0 + ss1);
+            if (lane == 0) partial[it & 1][warp] = ss;
+
+            if (m != m_cur) {  // uniform over the CTA; the loads overlap the barrier below
+                if constexpr (V == 1) {
+                    if (m == m_alt) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float tm = mul[0][e], ta = add[0][e];
+                            mul[0][e] = mul2[0][e]; add[0][e] = add2[0][e];
+                            mul2[0][e] = tm; add2[0][e] = ta;
+                        }
+                        m_alt = m_cur;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { mul2[0][e] = mul[0][e]; add2[0][e] = add[0][e]; }
+                        m_alt = m_cur;
+                        load_mod_row<V>(a, m, col, ok, mul, add);
+                    }
+                } else {
+                    load_mod_row<V>(a, m, col, ok, mul, add);
+                }
                 m_cur = m;
             }
-        }
 
-        uint16_t* dst = a.y + r * a.y_stride;
+            __syncthreads();
+            const float total = warp_sum(lane < nwarps ? partial[it & 1][lane] : 0.f);
+            const float inv_rms = rsqrtf(total * inv_hidden + a.eps);
+
+            uint16_t* dst = a.y + r * a.y_stride;
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            if (ok[i]) {
-                float o[8];
+            for (int i = 0; i < V; ++i) {
+                if (ok[i]) {
+                    float f[8], o[8];
+                    unpack8(xv[i], f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = fmaf(xf[i][e] * inv_rms * w[i][e], sc[i][e], sh[i][e]);
-                st_vec(dst + col[i] * 8, pack8(o));
+                    for (int e = 0; e < 8; ++e) o[e] = fmaf(f[e] * inv_rms, mul[i][e], add[i][e]);
+                    st_vec(dst + col[i] * 8, pack8(o));
+                }
             }
         }
-    }
-    cp_async_wait<0>();
+        cp_async_wait<0>();
     }  // nrows > 0
 
     // Fixed-valid mode: this CTA's share of the padded tail is written +0.0
@@ -202,7 +208,7 @@ bool choose_shape(int hidden, int* v, int* threads) {
     const int nvec = hidden / 8;
     for (int cand = 1; cand <= 8; cand *= 2) {
         const int t = (nvec + cand - 1) / cand;
-        if (t <= kMaxThreads) {
+        if (t <= (cand == 1 ? kMaxThreadsV1 : kMaxThreads)) {
             *v = cand;
             *threads = (t + 31) / 32 * 32;
             return true;

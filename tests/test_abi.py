@@ -111,8 +111,8 @@ def test_qk_validation(lib):
     assert qk(lib, D=120) == UNSUPPORTED
     assert qk(lib, D=8) == UNSUPPORTED
     assert qk(lib, D=1024, ist=3 * 8192, ost=3 * 8192, k=A + 2 * 8192, ko=B + 2 * 8192) == UNSUPPORTED
-    assert qk(lib, H=200, ist=3 * 200 * 128, ost=3 * 200 * 128, k=A + 2 * 200 * 128,
-              ko=B + 2 * 200 * 128) == UNSUPPORTED
+    assert passes_validation(lib, lambda: qk(lib, H=200, ist=3 * 200 * 128, ost=3 * 200 * 128,
+                                             k=A + 2 * 200 * 128, ko=B + 2 * 200 * 128))  # many heads: 2-D grid
     assert qk(lib, H=0) == INVALID
     assert qk(lib, theta=0.0) == INVALID
     assert qk(lib, theta=float("inf")) == INVALID

@@ -218,7 +218,9 @@ QK_CASES = [
     (65, 5, 96),       # 6 lanes per head in a group of 8
     (300, 24, 128),
     (77, 40, 128),
-    (19, 128, 128),    # most heads at head_dim 128 (4 head slots per thread)
+    (19, 128, 128),    # 4 heads per lane group, several head chunks
+    (13, 201, 128),    # odd head count: 1 head per lane group
+    (7, 300, 64),      # many heads: a 2-D grid of token runs x head chunks
     (11, 4, 256),
     (9, 2, 512),
 ]
