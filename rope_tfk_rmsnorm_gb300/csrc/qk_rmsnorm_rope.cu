@@ -108,12 +108,15 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
 #pragma unroll
         for (int e = 0; e < 8; ++e) { wa[e] = 0.f; wb[e] = 0.f; }
     }
-    // output address of head slot j: group h / hpg at group_stride, head h % hpg inside it
-    auto out_base = [&](int j) -> uint16_t* {
+    // output address of head slot j (token 0): group h / hpg at group_stride,
+    // head h % hpg inside the group's row; computed once, outside the token loop
+    uint16_t* out_base[HPT];
+#pragma unroll
+    for (int j = 0; j < HPT; ++j) {
         const int h = h0 + j;
         const int grp = h / a.heads_per_group;
-        return outp + (int64_t)grp * a.group_stride + (int64_t)(h - grp * a.heads_per_group) * D + lane * 8;
-    };
+        out_base[j] = outp + (int64_t)grp * a.group_stride + (int64_t)(h - grp * a.heads_per_group) * D + lane * 8;
+    }
 
     auto issue = [&](int row_in_run, int stage) {
         const uint16_t* src = src0 + (r0 + row_in_run) * a.in_stride;
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
                         oa[e] = fmaf(na, cs[e], -nb * sn[e]);
                         ob[e] = fmaf(nb, cs[e], na * sn[e]);
                     }
-                    uint16_t* o = out_base(j) + roff;
+                    uint16_t* o = out_base[j] + roff;
                     st_vec(o, pack8(oa));
                     st_vec(o + half, pack8(ob));
                 }
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             const int64_t roff = r * a.out_stride;
 #pragma unroll
             for (int j = 0; j < HPT; ++j) {
-                uint16_t* o = out_base(j) + roff;
+                uint16_t* o = out_base[j] + roff;
                 st_vec(o, zero);
                 st_vec(o + half, zero);
             }

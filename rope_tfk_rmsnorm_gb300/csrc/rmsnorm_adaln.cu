@@ -204,9 +204,13 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     }
 }
 
+// One vector per thread only for short rows (hidden < 2048, at most 256
+// threads): from 2048 on, two vectors per thread halve the CTA and let four
+// or five 64-register CTAs share an SM, which hides the per-row reduction
+// latency better than two big CTAs with the second cached modulation row.
 bool choose_shape(int hidden, int* v, int* threads) {
     const int nvec = hidden / 8;
-    for (int cand = 1; cand <= 8; cand *= 2) {
+    for (int cand = nvec >= 256 ? 2 : 1; cand <= 8; cand *= 2) {
         const int t = (nvec + cand - 1) / cand;
         if (t <= (cand == 1 ? kMaxThreadsV1 : kMaxThreads)) {
             *v = cand;
@@ -226,7 +230,7 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     const void* fn = reinterpret_cast<const void*>(&rmsnorm_adaln_kernel<V>);
     const int by_regs = blocks_per_sm(fn, threads, 0);
     if (by_regs <= 0) return cudaErrorInvalidConfiguration;
-    const int stages = pick_stages(by_regs >= 2 ? 2 : 1, row_bytes, 0);
+    const int stages = pick_stages(by_regs, row_bytes, 0);
     const size_t smem = (size_t)stages * row_bytes;
     const int per_sm = blocks_per_sm(fn, threads, smem);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
