@@ -14,8 +14,9 @@
 //   second half, so every rotate-half pair sits in one thread and needs no
 //   shuffle; the per-head sum of squares is a G-lane shuffle reduction.
 // - A group of G lanes owns HPT heads of the same tensor (q or k), so its
-//   weights stay in registers and the 8 cos/sin values a lane needs for a
-//   token are computed once and used for HPT heads.  Nothing is shared across
+//   weights stay in registers, and the 8 cos/sin values a lane needs for a
+//   token are computed once, folded with the weights, and used for HPT heads;
+//   the per-head 1/rms, a scalar, is applied after the rotation.  Nothing is shared across
 //   warps: there is no barrier anywhere in the token loop.
 // - The grid is 2-D: contiguous token runs x chunks of head groups (any head
 //   count fits), persistent over the token runs.  Each thread streams its own
@@ -144,12 +145,20 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             const int32_t p = p_next;
             if (it + 1 < nrows) p_next = __ldg(a.pos + r + 1);
 
-            float cs[8], sn[8];
+            // Weights folded into the rotation once per token for all HPT heads:
+            //   out[i]     = inv_rms * (v[i] * wa*c - v[i+D/2] * wb*s)
+            //   out[i+D/2] = inv_rms * (v[i+D/2] * wb*c + v[i] * wa*s)
+            // (the per-head 1/rms is a scalar, so it can be applied after the rotation).
+            float wac[8], wbs[8], wbc[8], was[8];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
                 const ulonglong2 f2 = *reinterpret_cast<const ulonglong2*>(fq + e);
-                rope_cos_sin(p, f2.x, cs[e], sn[e]);
-                rope_cos_sin(p, f2.y, cs[e + 1], sn[e + 1]);
+                float c0, s0, c1, s1;
+                rope_cos_sin(p, f2.x, c0, s0);
+                rope_cos_sin(p, f2.y, c1, s1);
+                wac[e] = wa[e] * c0; wbs[e] = wb[e] * s0; wbc[e] = wb[e] * c0; was[e] = wa[e] * s0;
+                wac[e + 1] = wa[e + 1] * c1; wbs[e + 1] = wb[e + 1] * s1;
+                wbc[e + 1] = wb[e + 1] * c1; was[e + 1] = wa[e + 1] * s1;
             }
 
             cp_async_wait_dyn(stages - 1);
@@ -181,10 +190,8 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
                     const float inv_rms = rsqrtf(ss[j] * inv_d + a.eps);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float na = va[e] * inv_rms * wa[e];
-                        const float nb = vb[e] * inv_rms * wb[e];
-                        oa[e] = fmaf(na, cs[e], -nb * sn[e]);
-                        ob[e] = fmaf(nb, cs[e], na * sn[e]);
+                        oa[e] = inv_rms * fmaf(va[e], wac[e], -vb[e] * wbs[e]);
+                        ob[e] = inv_rms * fmaf(vb[e], wbc[e], va[e] * was[e]);
                     }
                     uint16_t* o = out_base[j] + roff;
                     st_vec(o, pack8(oa));
