@@ -607,6 +607,29 @@ class Single:
             ev[1].record()
 
 
+def graph_ms(unit, reps: int) -> float:
+    """Device time per launch of `unit` replayed from one CUDA graph of `reps` launches:
+    the same kernels without host submission time (which dominates small workloads)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        unit.launch()                      # warm the library's per-device caches outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            unit.launch()
+    g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / reps
+
+
 def run_sweep(args, ranks: Ranks):
     """Every kernel on every workload at full size; one JSON line per workload (rank 0)."""
     import rope_tfk_rmsnorm_gb300 as tfk
@@ -649,16 +672,18 @@ def run_sweep(args, ranks: Ranks):
             rows_for = {}
         for u in units:
             total, per, _, _ = time_steps(u, K, W, ranks)
+            gms = graph_ms(u, K)
             if len(u.kernels) == 1:
                 ms = per[0]
                 rows = rows_for.get(u.kernels[0], wl.rows)
-                res[u.kernels[0]] = dict(_roof(u.bytes[0], ms, peak), tokens_per_s=rows / (ms * 1e-3))
+                res[u.kernels[0]] = dict(_roof(u.bytes[0], ms, peak), tokens_per_s=rows / (ms * 1e-3),
+                                         graph_ms=gms, graph_frac=_roof(u.bytes[0], gms, peak)["frac"])
             else:
                 ms = total / K
                 rows = vo.L if name == "valid_only" else wl.rows
                 res["chain" if name != "valid_only" else "valid_only_pipeline"] = dict(
                     _roof(sum(u.bytes), ms, peak), tokens_per_s=rows / (ms * 1e-3),
-                    kernels=u.kernels)
+                    graph_ms=gms, graph_frac=_roof(sum(u.bytes), gms, peak)["frac"], kernels=u.kernels)
         if ranks.rank == 0:
             print(json.dumps({"sweep": name, "workload": workload_config(wl)["workload"], "steps": K,
                               "peak_gbs": peak, "results": res}), flush=True)

@@ -80,12 +80,16 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     const int64_t r1 = a.rows * (int64_t)(tchunk + 1) / token_chunks;
     const int nrows = (int)(r1 - r0);
 
-    // fixed-point turn fractions of the D/2 frequencies, shared by the CTA
+    // Fixed-point turn fractions of the D/2 frequencies, shared by the CTA.
+    // Frequency i = 8*l + e belongs to lane l; it is stored at
+    // ((e/2)*L + l)*2 + e%2 so that the lanes of a warp read consecutive
+    // 16-byte pairs (no bank conflicts).
     for (int i = tid; i < half; i += nt) {
         const double f = pow((double)a.theta, -2.0 * (double)i / (double)D);
         double turns = f * 0.15915494309189533577;  // 1 / (2 pi)
         turns -= floor(turns);
-        ftab[i] = __double2ull_rz(turns * 18446744073709551616.0);  // * 2^64
+        const int l = i >> 3, e = i & 7;
+        ftab[((e >> 1) * L + l) * 2 + (e & 1)] = __double2ull_rz(turns * 18446744073709551616.0);  // * 2^64
     }
     __syncthreads();
 
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     uint16_t* outp = is_q ? a.q_out : a.k_out;
     const float* wsrc = is_q ? a.q_weight : a.k_weight;
     float wa[8], wb[8];
-    const uint64_t* fq = ftab + (active ? lane * 8 : 0);  // this lane's 8 frequencies, read per token
+    const ulonglong2* fq = reinterpret_cast<const ulonglong2*>(ftab) + (active ? lane : 0);  // stride L per pair
     if (active) {
         const float4 x0 = ld_f4(wsrc + lane * 8), x1 = ld_f4(wsrc + lane * 8 + 4);
         const float4 y0 = ld_f4(wsrc + half + lane * 8), y1 = ld_f4(wsrc + half + lane * 8 + 4);
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             float wac[8], wbs[8], wbc[8], was[8];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const ulonglong2 f2 = *reinterpret_cast<const ulonglong2*>(fq + e);
+                const ulonglong2 f2 = fq[(e >> 1) * L];
                 float c0, s0, c1, s1;
                 rope_cos_sin(p, f2.x, c0, s0);
                 rope_cos_sin(p, f2.y, c1, s1);
