@@ -101,27 +101,15 @@ int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes) {
     DeviceInfo di;
     if (device_info(&di) != cudaSuccess || stage_bytes <= 0) return 2;
     if (ctas_per_sm < 1) ctas_per_sm = 1;
-    // Fewer CTAs per SM leave more shared memory for each ring.  Take the most
-    // CTAs (<= what the registers allow) whose rings still keep kInflightPerSm
-    // bytes in flight; if none can, the pair with the most bytes in flight.
-    int best_stages = 2;
-    int64_t best_inflight = -1;
-    for (int c = ctas_per_sm; c >= 1; --c) {
-        const int64_t per_cta = (int64_t)di.max_smem_per_sm / c - 1024 - 1024 - extra_bytes;  // 1 KB reserved + static
-        int64_t s_max = per_cta / stage_bytes;
-        const int64_t optin_max = ((int64_t)di.max_smem_per_block_optin - 1024 - extra_bytes) / stage_bytes;
-        if (s_max > optin_max) s_max = optin_max;
-        if (s_max > 16) s_max = 16;
-        if (s_max < 2) continue;
-        const int64_t need = (kInflightPerSm + (int64_t)c * stage_bytes - 1) / ((int64_t)c * stage_bytes) + 1;
-        if (need <= s_max) return (int)(need < 2 ? 2 : need);
-        const int64_t inflight = (int64_t)c * (s_max - 1) * stage_bytes;
-        if (inflight > best_inflight) {
-            best_inflight = inflight;
-            best_stages = (int)s_max;
-        }
-    }
-    return best_stages;
+    int ahead = (kInflightPerSm + ctas_per_sm * stage_bytes - 1) / (ctas_per_sm * stage_bytes);
+    int stages = ahead + 1;
+    if (stages > 16) stages = 16;
+    // shared memory per SM (1 KB reserved per CTA) and per CTA (1 KB left for static shared memory)
+    const int64_t per_sm_budget = di.max_smem_per_sm / ctas_per_sm - 1024 - 1024;
+    while (stages > 2 && ((int64_t)stages * stage_bytes + extra_bytes > per_sm_budget ||
+                          (int64_t)stages * stage_bytes + extra_bytes > di.max_smem_per_block_optin - 1024))
+        --stages;
+    return stages < 2 ? 2 : stages;
 }
 
 }  // namespace tfk

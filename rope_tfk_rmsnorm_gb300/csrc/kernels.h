@@ -82,12 +82,10 @@ namespace tfk {
 // cached per device.  Returns 0 if the configuration cannot run.
 int blocks_per_sm(const void* func, int threads, size_t smem_bytes);
 
-// Depth of a cp.async staging ring (2..16 stages of `stage_bytes`): the
-// deepest ring that keeps about kInflightPerSm bytes in flight per SM for the
-// largest number of CTAs per SM (at most `ctas_per_sm`, the register limit)
-// whose rings fit in the SM's shared memory (`extra_bytes` of other dynamic
-// shared memory per CTA).  The launch then gets its CTAs per SM from the
-// occupancy at that shared-memory size.
+// Depth of a cp.async staging ring (2..16 stages of `stage_bytes`) that keeps
+// about kInflightPerSm bytes in flight per SM when `ctas_per_sm` CTAs share
+// an SM, within the shared memory of the SM and of one CTA (`extra_bytes` of
+// other dynamic shared memory per CTA).
 constexpr int kInflightPerSm = 112 * 1024;
 int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes);
 
