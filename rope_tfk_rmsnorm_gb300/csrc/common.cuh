@@ -68,6 +68,46 @@ __device__ __forceinline__ Vec8 pack8(const float f[8]) {
     return v;
 }
 
+// ---- packed fp32x2 arithmetic (sm_100+) ------------------------------------
+// Two fp32 values in one 64-bit register pair: lane 0 = the lower-addressed
+// element.  mul/fma .rn round each lane exactly like the scalar instruction,
+// at half the instruction count.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_split(f32x2 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// One bf16x2 word (element 2i in the low half) -> exact fp32x2.
+__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
+    return f2_make(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// fp32x2 -> one bf16x2 word, round to nearest even.
+__device__ __forceinline__ uint32_t f2_to_bf2(f32x2 v) {
+    float lo, hi;
+    f2_split(v, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
+
 // ---- cp.async staging (16 bytes per thread, bypassing L1) -----------------
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

@@ -86,7 +86,10 @@ int blocks_per_sm(const void* func, int threads, size_t smem_bytes);
 // about kInflightPerSm bytes in flight per SM when `ctas_per_sm` CTAs share
 // an SM, within the shared memory of the SM and of one CTA (`extra_bytes` of
 // other dynamic shared memory per CTA).
-constexpr int kInflightPerSm = 112 * 1024;
+#ifndef TFK_INFLIGHT_KB
+#define TFK_INFLIGHT_KB 112
+#endif
+constexpr int kInflightPerSm = TFK_INFLIGHT_KB * 1024;
 int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes);
 
 }  // namespace tfk

@@ -41,7 +41,14 @@ namespace {
 // 40-head token in one CTA at 4 heads per group; at most 102 registers so
 // that four CTAs share an SM.
 constexpr int kMaxThreads = 160;
-constexpr int kMinBlocks = 4;
+#ifndef TFK_A2_MIN_BLOCKS
+#define TFK_A2_MIN_BLOCKS 4
+#endif
+#ifndef TFK_A2_ROWS_PER_CTA
+#define TFK_A2_ROWS_PER_CTA 0  // 0: one persistent run of tokens per resident CTA
+#endif
+constexpr int kMinBlocks = TFK_A2_MIN_BLOCKS;
+constexpr int64_t kRowsPerCta = TFK_A2_ROWS_PER_CTA;
 
 __device__ __forceinline__ void rope_cos_sin(int32_t pos, uint64_t turn_fraction, float& c, float& s) {
     const uint64_t a = (uint64_t)(int64_t)pos * turn_fraction;        // mod 2^64 = mod one turn
@@ -102,26 +109,23 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     const uint16_t* src0 = (is_q ? a.q : a.k) + (int64_t)h0 * D + lane * 8;
     uint16_t* outp = is_q ? a.q_out : a.k_out;
     const float* wsrc = is_q ? a.q_weight : a.k_weight;
-    float wa[8], wb[8];
+    f32x2 wa[4], wb[4];  // weights of this lane's first-half / second-half elements, as pairs
     const ulonglong2* fq = reinterpret_cast<const ulonglong2*>(ftab) + (active ? lane : 0);  // stride L per pair
     if (active) {
         const float4 x0 = ld_f4(wsrc + lane * 8), x1 = ld_f4(wsrc + lane * 8 + 4);
         const float4 y0 = ld_f4(wsrc + half + lane * 8), y1 = ld_f4(wsrc + half + lane * 8 + 4);
-        wa[0] = x0.x; wa[1] = x0.y; wa[2] = x0.z; wa[3] = x0.w; wa[4] = x1.x; wa[5] = x1.y; wa[6] = x1.z; wa[7] = x1.w;
-        wb[0] = y0.x; wb[1] = y0.y; wb[2] = y0.z; wb[3] = y0.w; wb[4] = y1.x; wb[5] = y1.y; wb[6] = y1.z; wb[7] = y1.w;
+        wa[0] = f2_make(x0.x, x0.y); wa[1] = f2_make(x0.z, x0.w); wa[2] = f2_make(x1.x, x1.y); wa[3] = f2_make(x1.z, x1.w);
+        wb[0] = f2_make(y0.x, y0.y); wb[1] = f2_make(y0.z, y0.w); wb[2] = f2_make(y1.x, y1.y); wb[3] = f2_make(y1.z, y1.w);
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { wa[e] = 0.f; wb[e] = 0.f; }
+        for (int k = 0; k < 4; ++k) { wa[k] = 0ull; wb[k] = 0ull; }
     }
-    // output address of head slot j (token 0): group h / hpg at group_stride,
-    // head h % hpg inside the group's row; computed once, outside the token loop
-    uint16_t* out_base[HPT];
-#pragma unroll
-    for (int j = 0; j < HPT; ++j) {
-        const int h = h0 + j;
-        const int grp = h / a.heads_per_group;
-        out_base[j] = outp + (int64_t)grp * a.group_stride + (int64_t)(h - grp * a.heads_per_group) * D + lane * 8;
-    }
+    // Output address of the group's first head (token 0): output group
+    // h0 / hpg at group_stride, head h0 % hpg inside that group's row.  HPT
+    // divides hpg, so the group's HPT heads are consecutive in one output row.
+    const int ogrp = h0 / a.heads_per_group;
+    uint16_t* const out_base = outp + (int64_t)ogrp * a.group_stride +
+                               (int64_t)(h0 - ogrp * a.heads_per_group) * D + lane * 8;
 
     auto issue = [&](int row_in_run, int stage) {
         const uint16_t* src = src0 + (r0 + row_in_run) * a.in_stride;
@@ -153,16 +157,18 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             //   out[i]     = inv_rms * (v[i] * wa*c - v[i+D/2] * wb*s)
             //   out[i+D/2] = inv_rms * (v[i+D/2] * wb*c + v[i] * wa*s)
             // (the per-head 1/rms is a scalar, so it can be applied after the rotation).
-            float wac[8], wbs[8], wbc[8], was[8];
+            f32x2 wac[4], nwbs[4], wbc[4], was[4];  // wa*c, -(wb*s), wb*c, wa*s per element pair
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const ulonglong2 f2 = fq[(e >> 1) * L];
+            for (int k = 0; k < 4; ++k) {
+                const ulonglong2 fpair = fq[k * L];
                 float c0, s0, c1, s1;
-                rope_cos_sin(p, f2.x, c0, s0);
-                rope_cos_sin(p, f2.y, c1, s1);
-                wac[e] = wa[e] * c0; wbs[e] = wb[e] * s0; wbc[e] = wb[e] * c0; was[e] = wa[e] * s0;
-                wac[e + 1] = wa[e + 1] * c1; wbs[e + 1] = wb[e + 1] * s1;
-                wbc[e + 1] = wb[e + 1] * c1; was[e + 1] = wa[e + 1] * s1;
+                rope_cos_sin(p, fpair.x, c0, s0);
+                rope_cos_sin(p, fpair.y, c1, s1);
+                const f32x2 c2 = f2_make(c0, c1), s2 = f2_make(s0, s1), ns2 = f2_make(-s0, -s1);
+                wac[k] = f2_mul(wa[k], c2);
+                nwbs[k] = f2_mul(wb[k], ns2);
+                wbc[k] = f2_mul(wb[k], c2);
+                was[k] = f2_mul(wa[k], s2);
             }
 
             cp_async_wait_dyn(stages - 1);
@@ -172,13 +178,18 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             float ss[HPT];
 #pragma unroll
             for (int j = 0; j < HPT; ++j) {
-                float va[8], vb[8];
-                unpack8(ld_smem_vec(st + (j * 2 + 0) * nt), va);
-                unpack8(ld_smem_vec(st + (j * 2 + 1) * nt), vb);
-                float s0 = 0.f, s1 = 0.f;
+                const Vec8 a8 = ld_smem_vec(st + (j * 2 + 0) * nt), b8 = ld_smem_vec(st + (j * 2 + 1) * nt);
+                f32x2 sa = 0ull, sb = 0ull;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) { s0 = fmaf(va[e], va[e], s0); s1 = fmaf(vb[e], vb[e], s1); }
-                ss[j] = active ? s0 + s1 : 0.f;
+                for (int k = 0; k < 4; ++k) {
+                    const f32x2 va = bf2_to_f2(a8.w[k]), vb = bf2_to_f2(b8.w[k]);
+                    sa = f2_fma(va, va, sa);
+                    sb = f2_fma(vb, vb, sb);
+                }
+                float a0, a1, b0, b1;
+                f2_split(sa, a0, a1);
+                f2_split(sb, b0, b1);
+                ss[j] = active ? (a0 + a1) + (b0 + b1) : 0.f;
             }
             for (int o = G >> 1; o > 0; o >>= 1) {
 #pragma unroll
@@ -188,18 +199,19 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
                 const int64_t roff = r * a.out_stride;
 #pragma unroll
                 for (int j = 0; j < HPT; ++j) {
-                    float va[8], vb[8], oa[8], ob[8];
-                    unpack8(ld_smem_vec(st + (j * 2 + 0) * nt), va);
-                    unpack8(ld_smem_vec(st + (j * 2 + 1) * nt), vb);
+                    const Vec8 a8 = ld_smem_vec(st + (j * 2 + 0) * nt), b8 = ld_smem_vec(st + (j * 2 + 1) * nt);
                     const float inv_rms = rsqrtf(ss[j] * inv_d + a.eps);
+                    const f32x2 inv2 = f2_make(inv_rms, inv_rms);
+                    Vec8 oa, ob;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        oa[e] = inv_rms * fmaf(va[e], wac[e], -vb[e] * wbs[e]);
-                        ob[e] = inv_rms * fmaf(vb[e], wbc[e], va[e] * was[e]);
+                    for (int k = 0; k < 4; ++k) {
+                        const f32x2 va = bf2_to_f2(a8.w[k]), vb = bf2_to_f2(b8.w[k]);
+                        oa.w[k] = f2_to_bf2(f2_mul(f2_fma(va, wac[k], f2_mul(vb, nwbs[k])), inv2));
+                        ob.w[k] = f2_to_bf2(f2_mul(f2_fma(vb, wbc[k], f2_mul(va, was[k])), inv2));
                     }
-                    uint16_t* o = out_base[j] + roff;
-                    st_vec(o, pack8(oa));
-                    st_vec(o + half, pack8(ob));
+                    uint16_t* o = out_base + j * D + roff;
+                    st_vec(o, oa);
+                    st_vec(o + half, ob);
                 }
             }
         }
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             const int64_t roff = r * a.out_stride;
 #pragma unroll
             for (int j = 0; j < HPT; ++j) {
-                uint16_t* o = out_base[j] + roff;
+                uint16_t* o = out_base + j * D + roff;
                 st_vec(o, zero);
                 st_vec(o + half, zero);
             }
@@ -226,11 +238,14 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     }
 }
 
-bool choose_layout(int n_heads, int head_dim, Layout* lay) {
+// heads_per_group: heads per output group (n_heads, or n_heads / sp_degree in
+// the Ulysses layout); a lane group's heads never straddle two output groups.
+bool choose_layout(int n_heads, int head_dim, int heads_per_group, Layout* lay) {
     if (head_dim < 16 || head_dim > 512 || head_dim % 16 != 0 || n_heads < 1 || n_heads > (1 << 20)) return false;
+    if (heads_per_group < 1 || n_heads % heads_per_group != 0) return false;
     int L = head_dim / 16, G = 1;
     while (G < L) G <<= 1;
-    int hpt = n_heads % 4 == 0 ? 4 : (n_heads % 2 == 0 ? 2 : 1);
+    int hpt = heads_per_group % 4 == 0 ? 4 : (heads_per_group % 2 == 0 ? 2 : 1);
     const int64_t groups = 2LL * n_heads / hpt;
     // as few head chunks as possible with at most kMaxThreads threads per CTA
     const int64_t per_cta = kMaxThreads / G;
@@ -262,6 +277,10 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
     // token runs: enough CTAs for every SM, and no more runs than rows to work on
     int64_t want = ((int64_t)per_sm * di.sm_count + lay.head_chunks - 1) / lay.head_chunks;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
+    if constexpr (kRowsPerCta > 0) {  // fixed-size chunks instead of one persistent run per CTA
+        const int64_t chunks = (work + kRowsPerCta - 1) / (kRowsPerCta > 0 ? kRowsPerCta : 1);
+        if (chunks > want) want = chunks;
+    }
     if (want > work) want = work;
     if (want < 1) return cudaSuccess;
     const int64_t grid = want * lay.head_chunks;
@@ -274,12 +293,12 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
 
 bool qk_rope_supported(int n_heads, int head_dim) {
     Layout lay;
-    return choose_layout(n_heads, head_dim, &lay);
+    return choose_layout(n_heads, head_dim, n_heads, &lay);
 }
 
 cudaError_t launch_qk_rmsnorm_rope(const QkRopeArgs& a, cudaStream_t stream) {
     Layout lay;
-    if (!choose_layout(a.n_heads, a.head_dim, &lay)) return cudaErrorInvalidValue;
+    if (!choose_layout(a.n_heads, a.head_dim, a.heads_per_group, &lay)) return cudaErrorInvalidValue;
     switch (lay.hpt) {
         case 1: return launch_h<1>(a, lay, stream);
         case 2: return launch_h<2>(a, lay, stream);

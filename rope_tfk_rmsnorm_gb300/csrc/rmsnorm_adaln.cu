@@ -27,6 +27,10 @@ namespace {
 
 constexpr int kMaxThreads = 512;
 constexpr int kMaxThreadsV1 = 384;
+#ifndef TFK_A1_ROWS_PER_CTA
+#define TFK_A1_ROWS_PER_CTA 0  // 0: one persistent run of rows per resident CTA
+#endif
+constexpr int64_t kRowsPerCta = TFK_A1_ROWS_PER_CTA;
 
 // Combined modulation of the columns a thread owns for modulation row m:
 //   mul = w * (1 + scale[m]),  add = shift[m]
@@ -236,6 +240,10 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)per_sm * di.sm_count;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
+    if constexpr (kRowsPerCta > 0) {  // fixed-size chunks instead of one persistent run per CTA
+        const int64_t chunks = (work + kRowsPerCta - 1) / (kRowsPerCta > 0 ? kRowsPerCta : 1);
+        if (chunks > grid) grid = chunks;
+    }
     if (grid > work) grid = work;
     if (grid < 1) return cudaSuccess;
     rmsnorm_adaln_kernel<V><<<(unsigned)grid, threads, smem, stream>>>(a, stages);
