@@ -24,13 +24,16 @@
 //   ahead, and reads back only the slots it copied itself.
 // - Angles are reduced exactly in integer arithmetic: theta^(-2i/D)/(2 pi) is
 //   held as a 64-bit fixed-point fraction of a turn F_i (computed once per
-//   CTA in fp64), pos * F_i mod 2^64 is the angle's fraction of a turn, and
+//   launch in fp64 on the host side and passed by value), pos * F_i mod 2^64
+//   is the angle's fraction of a turn, and
 //   its top 32 bits give an fp32 angle in [-pi, pi).  On that range the
 //   hardware sin/cos approximations are accurate to about 4e-7 absolute, so
 //   no fp64 and no range reduction is needed per token.
 // - The output can go straight into the Ulysses all-to-all send layout
 //   [groups][rows][heads/groups][D] ("Fuse Q/K RMSNorm, RoPE, and Ulysses
 //   packing", TeleFuser PR #38 section 2): only the store address changes.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -62,6 +65,30 @@ __device__ __forceinline__ void rope_cos_sin(int32_t pos, uint64_t turn_fraction
     __sincosf(angle, &s, &c);
 }
 
+// Fixed-point turn fractions of the D/2 RoPE frequencies of one launch,
+// frac(theta^(-2i/D) / (2 pi)) * 2^64, in the lane-interleaved layout read by
+// the kernel (frequency i = 8*l + e of lane l at ((e/2)*L + l)*2 + e%2).  They
+// depend only on (theta, head_dim), so they are computed once per launch, in
+// double precision, and passed by value.
+struct RopeTable {
+    unsigned long long f[256];
+};
+
+RopeTable make_rope_table(double theta, int head_dim) {
+    RopeTable t;
+    const int half = head_dim / 2, L = head_dim / 16;
+    for (int i = 0; i < half; ++i) {
+        const double f = std::pow(theta, -2.0 * (double)i / (double)head_dim);
+        double turns = f * 0.15915494309189533577;  // 1 / (2 pi)
+        turns -= std::floor(turns);
+        double scaled = std::ldexp(turns, 64);
+        if (scaled >= 18446744073709551615.0) scaled = 18446744073709549568.0;  // largest double below 2^64
+        const int l = i >> 3, e = i & 7;
+        t.f[((e >> 1) * L + l) * 2 + (e & 1)] = (unsigned long long)scaled;
+    }
+    return t;
+}
+
 struct Layout {
     int hpt;          // heads per lane group (all of one tensor)
     int lanes;        // G
@@ -72,7 +99,8 @@ struct Layout {
 
 template <int HPT>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const QkRopeArgs a, const Layout lay,
-                                                              const int token_chunks, const int stages) {
+                                                              const int token_chunks, const int stages,
+                                                              const __grid_constant__ RopeTable tab) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int nt = blockDim.x;
     const int tid = threadIdx.x;
@@ -92,17 +120,9 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     const int64_t r1 = a.rows * (int64_t)(tchunk + 1) / token_chunks;
     const int nrows = (int)(r1 - r0);
 
-    // Fixed-point turn fractions of the D/2 frequencies, shared by the CTA.
-    // Frequency i = 8*l + e belongs to lane l; it is stored at
-    // ((e/2)*L + l)*2 + e%2 so that the lanes of a warp read consecutive
-    // 16-byte pairs (no bank conflicts).
-    for (int i = tid; i < half; i += nt) {
-        const double f = pow((double)a.theta, -2.0 * (double)i / (double)D);
-        double turns = f * 0.15915494309189533577;  // 1 / (2 pi)
-        turns -= floor(turns);
-        const int l = i >> 3, e = i & 7;
-        ftab[((e >> 1) * L + l) * 2 + (e & 1)] = __double2ull_rz(turns * 18446744073709551616.0);  // * 2^64
-    }
+    // The launch's frequency table into shared memory (lane-interleaved layout:
+    // the lanes of a warp then read consecutive 16-byte pairs, no bank conflicts).
+    for (int i = tid; i < half; i += nt) ftab[i] = tab.f[i];
     __syncthreads();
 
     const int lane = tid % G;
@@ -290,7 +310,16 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
     if (want < 1) return cudaSuccess;
     const int64_t grid = want * lay.head_chunks;
     if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-    qk_rope_kernel<HPT><<<(unsigned)grid, lay.threads, smem, stream>>>(a, lay, (int)want, stages);
+    // the table of the last (theta, head_dim) seen on this host thread is kept
+    thread_local float last_theta = -1.0f;
+    thread_local int last_dim = 0;
+    thread_local RopeTable table;
+    if (a.theta != last_theta || a.head_dim != last_dim) {
+        table = make_rope_table(a.theta, a.head_dim);
+        last_theta = a.theta;
+        last_dim = a.head_dim;
+    }
+    qk_rope_kernel<HPT><<<(unsigned)grid, lay.threads, smem, stream>>>(a, lay, (int)want, stages, table);
     return cudaGetLastError();
 }
 
