@@ -409,3 +409,18 @@ def test_ulysses_degree_one_is_identity_and_unpack_inverts_pack():
     assert np.array_equal(oracle.ulysses_pack(x, 6, 32, 1).reshape(7, -1), x)
     for P in (1, 2, 3, 6):
         assert np.array_equal(oracle.ulysses_unpack(oracle.ulysses_pack(x, 6, 32, P), 6, 32, P), x)
+
+
+def test_fixed_valid_oracle_is_the_plain_definition_then_zeros():
+    x, w, shift, scale, idx = _mod_inputs(40, 128, 3)
+    full = oracle.rmsnorm_adaln_indexed(x, w, shift, scale, idx, 1e-6)
+    assert np.array_equal(oracle.rmsnorm_adaln_fixed_valid(x, 40, w, shift, scale, idx, 1e-6), full)
+    part = oracle.rmsnorm_adaln_fixed_valid(x, 25, w, shift, scale, idx, 1e-6)
+    assert np.array_equal(part[:25], full[:25]) and np.all(part[25:] == 0.0)
+    assert np.all(oracle.round_bf16(part[25:]) == 0x0000)                 # +0.0, not -0.0
+    q = bf16(np.random.default_rng(2).standard_normal((40, 2 * 64)))
+    wq = np.ones(64, np.float32)
+    pos = np.arange(40, dtype=np.int32)
+    qf, kf = oracle.qk_rmsnorm_rope_neox(q, q, wq, wq, pos, 2, 64, 10000.0, 1e-6)
+    qp, kp = oracle.qk_rmsnorm_rope_neox_fixed_valid(q, q, 30, wq, wq, pos, 2, 64, 10000.0, 1e-6)
+    assert np.array_equal(qp[:30], qf[:30]) and np.all(qp[30:] == 0.0) and np.array_equal(kp[:30], kf[:30])

@@ -579,3 +579,25 @@ def test_ulysses_pack_unpack_bit_exact(cuda, rows, H, D, P, stride_pad):
     back.check()
     src.check()
     assert np.array_equal(back.host(), x)
+
+
+@pytest.mark.parametrize("P", [4, 8])
+def test_qk_ulysses_full_size_sampled(cuda, P):
+    """The fused Ulysses packing on the 75,600-token workload (40 heads: 10 or 5 heads per
+    rank), sampled rows against the oracle."""
+    wl = synth.get("large")
+    p, pd = _params_dev(wl)
+    rows = synth.sample_rows(wl, 96)
+    _, dev = _inputs_dev(wl, ["q", "k"])
+    qs, ks = tfk.tfk_qk_rmsnorm_rope_neox_ulysses(dev["q"], dev["k"], pd["w_q"], pd["w_k"],
+                                                  i32_dev(synth.positions(wl)), wl.n_heads, wl.head_dim, P)
+    torch.cuda.synchronize()
+    sel = torch.from_numpy(rows).cuda()
+    got_q = to_host(qs[:, sel])                    # [P, sample, H/P, D]
+    got_k = to_host(ks[:, sel])
+    del dev, qs, ks
+    rq, rk = ora_qk(synth.activation(wl, "q", rows=rows), synth.activation(wl, "k", rows=rows), p["w_q"], p["w_k"],
+                    synth.positions(wl, rows), wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    check_close(got_q.reshape(-1), oracle.ulysses_pack(rq, wl.n_heads, wl.head_dim, P).reshape(-1), f"ulysses q P={P}")
+    check_close(got_k.reshape(-1), oracle.ulysses_pack(rk, wl.n_heads, wl.head_dim, P).reshape(-1), f"ulysses k P={P}")
+    torch.cuda.empty_cache()

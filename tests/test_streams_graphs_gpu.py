@@ -1,0 +1,113 @@
+"""The entry points as a caller uses them beyond the default stream: on side
+streams, from several host threads at once, and captured into a CUDA graph and
+replayed; results must equal the ones of a plain launch bit for bit."""
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import rope_tfk_rmsnorm_gb300 as tfk
+import synth
+from helpers import f32_dev, i32_dev, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(rows=3000, name="sg"):
+    wl = synth.custom(name, rows, 3072, 24, 128, 8192, n_mod=4, n_audio=rows // 8)
+    p = {k: f32_dev(v) for k, v in synth.params(wl).items()}
+    d = {t: to_dev(synth.activation(wl, t)) for t in ("x", "q", "k", "gate_up")}
+    d["idx"] = i32_dev(synth.mod_index(wl) % 4)
+    d["pos"] = i32_dev(synth.positions(wl))
+    return wl, p, d
+
+
+def _chain(wl, p, d, stream=None):
+    y = tfk.tfk_rmsnorm_adaln_indexed(d["x"], p["w"], p["shift"], p["scale"], d["idx"], wl.eps, stream=stream)
+    qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(d["q"], d["k"], p["w_q"], p["w_k"], d["pos"], wl.n_heads, wl.head_dim,
+                                         wl.theta, wl.eps, stream=stream)
+    o = tfk.tfk_swiglu(d["gate_up"], stream=stream)
+    return y, qo, ko, o
+
+
+def _bits(ts):
+    return [to_host(t) for t in ts]
+
+
+def test_side_streams_give_the_same_bits(cuda):
+    wl, p, d = _problem()
+    ref = _bits(_chain(wl, p, d))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            outs = _chain(wl, p, d, stream=s)
+        s.synchronize()
+        for a, b in zip(_bits(outs), ref):
+            assert np.array_equal(a, b)
+
+
+def test_concurrent_host_threads(cuda):
+    wl, p, d = _problem(name="threads")
+    ref = _bits(_chain(wl, p, d))
+    torch.cuda.synchronize()
+    results, errors = {}, []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(cuda)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    outs = _chain(wl, p, d, stream=s)
+            s.synchronize()
+            results[i] = _bits(outs)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(4):
+        for a, b in zip(results[i], ref):
+            assert np.array_equal(a, b)
+
+
+def test_graph_capture_and_replay(cuda):
+    wl, p, d = _problem(name="graph")
+    ref = _bits(_chain(wl, p, d))
+    out = {
+        "y": torch.empty_like(d["x"]),
+        "q": torch.empty_like(d["q"]), "k": torch.empty_like(d["k"]),
+        "o": torch.empty((wl.rows, wl.ffn), dtype=torch.bfloat16, device=cuda),
+    }
+
+    def launch():
+        tfk.tfk_rmsnorm_adaln_indexed(d["x"], p["w"], p["shift"], p["scale"], d["idx"], wl.eps, out=out["y"])
+        tfk.tfk_qk_rmsnorm_rope_neox(d["q"], d["k"], p["w_q"], p["w_k"], d["pos"], wl.n_heads, wl.head_dim,
+                                     wl.theta, wl.eps, q_out=out["q"], k_out=out["k"])
+        tfk.tfk_swiglu(d["gate_up"], out=out["o"])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        launch()                                   # warm the library's per-device caches
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for t in out.values():
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch()
+    for _ in range(2):
+        for t in out.values():
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(_bits([out["y"], out["q"], out["k"], out["o"]]), ref):
+            assert np.array_equal(a, b)
