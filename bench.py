@@ -670,6 +670,18 @@ def run_sweep(args, ranks: Ranks):
                                                       q_out=ch.out["q"], k_out=ch.out["k"]),
                  lambda: tfk.tfk_swiglu(ch.d["gate_up"], out=ch.out["o"])])] + [ch]
             rows_for = {}
+            if name == "large":  # the Ulysses layouts, 8-way (5 heads per rank)
+                P = 8
+                qk_bytes = bytes_qk(wl.rows, wl.n_heads, wl.head_dim)
+                send_q = torch.empty((P, wl.rows, wl.n_heads // P, wl.head_dim), dtype=torch.bfloat16, device=device)
+                send_k = torch.empty_like(send_q)
+                units.insert(3, Single("qk_rmsnorm_rope_ulysses_p8", qk_bytes, lambda: tfk.tfk_qk_rmsnorm_rope_neox_ulysses(
+                    ch.d["q"], ch.d["k"], ch.params["w_q"], ch.params["w_k"], ch.d["pos"], wl.n_heads, wl.head_dim, P,
+                    wl.theta, wl.eps, q_send=send_q, k_send=send_k)))
+                units.insert(4, Single("ulysses_pack_p8", 4 * wl.n_heads * wl.head_dim * wl.rows,
+                                       lambda: tfk.tfk_ulysses_pack(ch.d["q"], wl.n_heads, wl.head_dim, P, dst=send_q)))
+                units.insert(5, Single("ulysses_unpack_p8", 4 * wl.n_heads * wl.head_dim * wl.rows,
+                                       lambda: tfk.tfk_ulysses_unpack(send_q, wl.n_heads, wl.head_dim, P, dst=ch.out["q"])))
         for u in units:
             total, per, _, _ = time_steps(u, K, W, ranks)
             gms = graph_ms(u, K)

@@ -14,17 +14,6 @@ struct alignas(16) Vec8 {
     uint32_t w[4];
 };
 
-// Streaming 16-byte load that does not allocate in L1 (each activation byte is
-// read once).  Plain (coherent) load: the in-place variants write the same
-// addresses afterwards from the same thread.
-__device__ __forceinline__ Vec8 ld_stream(const void* p) {
-    Vec8 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                 : "l"(p));
-    return v;
-}
-
 // Read-only 16-byte load through the non-coherent path (inputs never written
 // by the kernel).
 __device__ __forceinline__ Vec8 ld_ro(const void* p) {
@@ -165,14 +154,6 @@ __device__ __forceinline__ Vec8 ld_smem_vec(const void* p) {
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-
-// Sum over aligned groups of G lanes (G a power of two <= 32).
-template <int G>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
 }
 

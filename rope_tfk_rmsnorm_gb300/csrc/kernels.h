@@ -73,10 +73,6 @@ cudaError_t launch_zero_tail_merge(const uint16_t* compact, uint16_t* padded, in
 bool rmsnorm_adaln_supported(int hidden);
 bool qk_rope_supported(int n_heads, int head_dim);
 
-}  // namespace tfk
-
-namespace tfk {
-
 // Resident CTAs per SM for `func` at this block size and dynamic shared
 // memory (raising the function's dynamic shared-memory limit when needed);
 // cached per device.  Returns 0 if the configuration cannot run.

@@ -145,12 +145,16 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
 #pragma unroll
         for (int k = 0; k < 4; ++k) { wa[k] = 0ull; wb[k] = 0ull; }
     }
-    // Output address of the group's first head (token 0): output group
-    // h0 / hpg at group_stride, head h0 % hpg inside that group's row.  HPT
-    // divides hpg, so the group's HPT heads are consecutive in one output row.
-    const int ogrp = h0 / a.heads_per_group;
-    uint16_t* const out_base = outp + (int64_t)ogrp * a.group_stride +
-                               (int64_t)(h0 - ogrp * a.heads_per_group) * D + lane * 8;
+    // Output offset of each of the group's heads (token 0): output group
+    // h / hpg at group_stride, head h % hpg inside that group's row (in the
+    // Ulysses layout consecutive heads may fall in different groups).
+    int64_t out_off[HPT];
+#pragma unroll
+    for (int j = 0; j < HPT; ++j) {
+        const int h = h0 + j;
+        const int ogrp = h / a.heads_per_group;
+        out_off[j] = (int64_t)ogrp * a.group_stride + (int64_t)(h - ogrp * a.heads_per_group) * D + lane * 8;
+    }
 
     auto issue = [&](int row_in_run, int stage) {
         const uint16_t* src = src0 + (r0 + row_in_run) * a.in_stride;
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
                         oa.w[k] = f2_to_bf2(f2_mul(f2_fma(va, wac[k], f2_mul(vb, nwbs[k])), inv2));
                         ob.w[k] = f2_to_bf2(f2_mul(f2_fma(vb, wbc[k], f2_mul(va, was[k])), inv2));
                     }
-                    uint16_t* o = out_base + j * D + roff;
+                    uint16_t* o = outp + out_off[j] + roff;
                     st_vec(o, oa);
                     st_vec(o + half, ob);
                 }
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             const int64_t roff = r * a.out_stride;
 #pragma unroll
             for (int j = 0; j < HPT; ++j) {
-                uint16_t* o = out_base + j * D + roff;
+                uint16_t* o = outp + out_off[j] + roff;
                 st_vec(o, zero);
                 st_vec(o + half, zero);
             }
@@ -264,13 +268,14 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
 }
 
 // heads_per_group: heads per output group (n_heads, or n_heads / sp_degree in
-// the Ulysses layout); a lane group's heads never straddle two output groups.
+// the Ulysses layout).  A lane group's heads are all q or all k (hpt divides
+// n_heads); they may fall in different output groups.
 bool choose_layout(int n_heads, int head_dim, int heads_per_group, Layout* lay) {
     if (head_dim < 16 || head_dim > 512 || head_dim % 16 != 0 || n_heads < 1 || n_heads > (1 << 20)) return false;
     if (heads_per_group < 1 || n_heads % heads_per_group != 0) return false;
     int L = head_dim / 16, G = 1;
     while (G < L) G <<= 1;
-    int hpt = heads_per_group % 4 == 0 ? 4 : (heads_per_group % 2 == 0 ? 2 : 1);
+    int hpt = n_heads % 4 == 0 ? 4 : (n_heads % 2 == 0 ? 2 : 1);
     const int64_t groups = 2LL * n_heads / hpt;
     // as few head chunks as possible with at most kMaxThreads threads per CTA
     const int64_t per_cta = kMaxThreads / G;

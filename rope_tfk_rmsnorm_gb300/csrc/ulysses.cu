@@ -8,8 +8,9 @@
 // unpack: the inverse, [G][rows][H/G][D] -> [rows, row_stride].
 //
 // A bit-exact permutation, HBM-bound (2 bytes read + 2 written per element).
-// One CTA walks whole token rows; the row side of every access is
-// contiguous, the head side is contiguous in runs of D values.
+// Persistent CTAs over runs of rows; at every row the row side of a warp's
+// accesses is contiguous and the grouped side contiguous in runs of
+// (heads per group) * D values.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,27 +18,41 @@ namespace tfk {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kRowsPerStep = 4;
 
+// Each thread owns fixed 16-byte column vectors of the row layout (their
+// head / group coordinates are computed once) and walks this CTA's run of
+// rows, kRowsPerStep rows at a time with independent loads in flight.
 __global__ void __launch_bounds__(kThreads) relayout_kernel(const uint16_t* __restrict__ src,
                                                             uint16_t* __restrict__ dst, int64_t row_stride,
                                                             int64_t rows, int n_heads, int head_dim,
                                                             int heads_per_group, int pack) {
     const int vec_per_head = head_dim >> 3;
     const int vec_per_row = n_heads * vec_per_head;
-    const int64_t group_elems = rows * (int64_t)heads_per_group * head_dim;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        for (int v = threadIdx.x; v < vec_per_row; v += kThreads) {
-            const int h = v / vec_per_head;
-            const int e = v - h * vec_per_head;
-            const int g = h / heads_per_group;
-            const int hl = h - g * heads_per_group;
-            const int64_t row_off = r * row_stride + (int64_t)v * 8;
-            const int64_t grp_off = g * group_elems + (r * heads_per_group + hl) * (int64_t)head_dim + e * 8;
-            if (pack)
-                st_vec(dst + grp_off, ld_ro(src + row_off));
-            else
-                st_vec(dst + row_off, ld_ro(src + grp_off));
+    const int64_t grp_row = (int64_t)heads_per_group * head_dim;  // elements per row inside a group
+    const int64_t group_elems = rows * grp_row;
+    const int64_t r0 = rows * (int64_t)blockIdx.x / gridDim.x;
+    const int64_t r1 = rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
+    for (int v = threadIdx.x; v < vec_per_row; v += kThreads) {
+        const int h = v / vec_per_head;
+        const int e = v - h * vec_per_head;
+        const int g = h / heads_per_group;
+        const int hl = h - g * heads_per_group;
+        const int64_t row_col = (int64_t)v * 8;                                   // row layout
+        const int64_t grp_col = g * group_elems + (int64_t)hl * head_dim + e * 8;  // grouped layout
+        const int64_t row_step = pack ? row_stride : grp_row;
+        const int64_t dst_step = pack ? grp_row : row_stride;
+        const uint16_t* s0 = src + (pack ? row_col : grp_col);
+        uint16_t* d0 = dst + (pack ? grp_col : row_col);
+        int64_t r = r0;
+        for (; r + kRowsPerStep <= r1; r += kRowsPerStep) {
+            Vec8 t[kRowsPerStep];
+#pragma unroll
+            for (int k = 0; k < kRowsPerStep; ++k) t[k] = ld_ro(s0 + (r + k) * row_step);
+#pragma unroll
+            for (int k = 0; k < kRowsPerStep; ++k) st_vec(d0 + (r + k) * dst_step, t[k]);
         }
+        for (; r < r1; ++r) st_vec(d0 + r * dst_step, ld_ro(s0 + r * row_step));
     }
 }
 
@@ -51,7 +66,7 @@ cudaError_t launch_ulysses_relayout(const uint16_t* src, uint16_t* dst, int64_t 
     const void* fn = reinterpret_cast<const void*>(&relayout_kernel);
     const int per_sm = blocks_per_sm(fn, kThreads, 0);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-    int64_t grid = (int64_t)per_sm * di.sm_count * 4;
+    int64_t grid = (int64_t)per_sm * di.sm_count;
     if (grid > rows) grid = rows;
     relayout_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(src, dst, row_stride, rows, n_heads, head_dim,
                                                              n_heads / groups, pack ? 1 : 0);
