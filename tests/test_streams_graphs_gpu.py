@@ -111,3 +111,19 @@ def test_graph_capture_and_replay(cuda):
         torch.cuda.synchronize()
         for a, b in zip(_bits([out["y"], out["q"], out["k"], out["o"]]), ref):
             assert np.array_equal(a, b)
+
+
+def test_a_failed_call_leaves_the_next_launch_unaffected(cuda):
+    """After an injected launch failure, and after a call rejected on the host,
+    the next call launches normally and computes the same bits."""
+    wl, p, d = _problem(rows=512, name="after_error")
+    ref = _bits(_chain(wl, p, d))
+    lib = tfk.load()
+    assert lib.tfk_debug_fail_next_launch(700) == 0
+    with pytest.raises(tfk.TfkError) as e:
+        tfk.tfk_swiglu(d["gate_up"])
+    assert e.value.status == 4 and "[injected]" in str(e.value)
+    with pytest.raises(tfk.TfkError):
+        tfk.tfk_swiglu(d["gate_up"], ffn=12)          # rejected on the host
+    for a, b in zip(_bits(_chain(wl, p, d)), ref):
+        assert np.array_equal(a, b)
