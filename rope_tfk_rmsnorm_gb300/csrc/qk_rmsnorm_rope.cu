@@ -42,18 +42,18 @@ namespace {
 
 // 160 threads = 20 lane groups of 8 (head_dim 128): all 80 q/k heads of a
 // 40-head token in one CTA at 4 heads per group, at most 136 registers (three
-// CTAs per SM at least).  CTAs take 8-token chunks and the hardware block
+// CTAs per SM at least).  CTAs take 4-token chunks and the hardware block
 // scheduler balances the chunks over the SMs: measured on the GB300 at 75,600
-// tokens this reaches ~100% of the measured HBM peak, against 88% for one
+// tokens this reaches ~103% of the measured HBM peak, against 88% for one
 // persistent run of ~166 tokens per CTA (whose static split leaves some SMs
-// idle at the end) and 85% with a 102-register cap; 8-token chunks measured
-// 0.5-1.5% above 16 and 24.
+// idle at the end) and 85% with a 102-register cap; 4-token chunks measured
+// 1-4% above 8 on all four workload shapes, 8 above 16 and 24.
 constexpr int kMaxThreads = 160;
 #ifndef TFK_A2_MIN_BLOCKS
 #define TFK_A2_MIN_BLOCKS 3
 #endif
 #ifndef TFK_A2_ROWS_PER_CTA
-#define TFK_A2_ROWS_PER_CTA 8  // 0: one persistent run of tokens per resident CTA
+#define TFK_A2_ROWS_PER_CTA 4  // 0: one persistent run of tokens per resident CTA
 #endif
 constexpr int kMinBlocks = TFK_A2_MIN_BLOCKS;
 constexpr int64_t kRowsPerCta = TFK_A2_ROWS_PER_CTA;
