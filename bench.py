@@ -330,7 +330,8 @@ class ValidOnly:
 
 def time_steps(work, steps: int, warmup: int, ranks: Ranks):
     """W untimed steps, then exactly `steps` timed steps between barriers and syncs.
-    Returns (total ms on the device, per-kernel mean ms, wall t0, wall t1)."""
+    Returns (total ms on the device, per-kernel mean ms, wall t0, wall t1, per-kernel
+    {p10, p50, p90} ms over the timed steps)."""
     n_ev = len(work.kernels) + 1
     for _ in range(warmup):
         work.launch()
@@ -348,9 +349,10 @@ def time_steps(work, steps: int, warmup: int, ranks: Ranks):
     t1 = time.time()
     ranks.barrier()
     total = start.elapsed_time(end)
-    per_kernel = [statistics.fmean(evs[s][j].elapsed_time(evs[s][j + 1]) for s in range(steps))
-                  for j in range(n_ev - 1)]
-    return total, per_kernel, t0, t1
+    samples = [[evs[s][j].elapsed_time(evs[s][j + 1]) for s in range(steps)] for j in range(n_ev - 1)]
+    per_kernel = [statistics.fmean(v) for v in samples]
+    dist = [{f"p{q}": float(np.percentile(v, q)) for q in (10, 50, 90)} for v in samples]
+    return total, per_kernel, t0, t1, dist
 
 
 # ---------------------------------------------------------------------------
@@ -387,10 +389,13 @@ def cpu_baseline(wl, seconds: float) -> dict:
         spent += _oracle_chain(oracle, wl, rows, p, threads)
         done += len(rows)
         start = (start + stride) % max(1, wl.rows - chunk)
+    one = min(64, wl.rows)  # the same oracle on one thread, on a smaller sample
+    one_s = _oracle_chain(oracle, wl, rng_rows[:one], p, 1)
     return {"value": done / spent, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{done} rows of the {wl.name} workload ({wl.rows} rows) in chunks of {chunk}, "
                       f"{spent:.1f} s of timed fp64 oracle work (RMSNorm+AdaLN, Q/K RMSNorm+RoPE, SwiGLU, "
-                      f"bf16 rounding); input generation untimed"}
+                      f"bf16 rounding); input generation untimed",
+            "value_1thread": one / one_s, "sample_1thread": f"the first {one} rows on 1 thread"}
 
 
 def run_reference(args, ranks: Ranks) -> dict | None:
@@ -542,13 +547,14 @@ def run_tfk(args, ranks: Ranks) -> dict | None:
     chain = Chain(tfk, wl, device)
     torch.cuda.synchronize()
     sampler = ClockSampler(_smi_id(device)) if ranks.rank == 0 else None
-    total_ms, per_kernel, t0, t1 = time_steps(chain, K, W, ranks)
+    total_ms, per_kernel, t0, t1, dist = time_steps(chain, K, W, ranks)
     clocks = sampler.stop(t0, t1) if sampler else None
     max_s = ranks.max(total_ms / 1e3)
     value = aggregate(wl.rows * K, ranks.world, max_s)
     chain_bytes = sum(chain.bytes)
-    kernels = {n: dict(_roof(b, ms, peak), tokens_per_s=wl.rows / (ms * 1e-3))
-               for n, b, ms in zip(chain.kernels, chain.bytes, per_kernel)}
+    kernels = {n: dict(_roof(b, ms, peak), tokens_per_s=wl.rows / (ms * 1e-3),
+                       ms_p10=d["p10"], ms_median=d["p50"], ms_p90=d["p90"])
+               for n, b, ms, d in zip(chain.kernels, chain.bytes, per_kernel, dist)}
     dom = max(range(len(per_kernel)), key=lambda j: per_kernel[j])
     dom_name = chain.kernels[dom]
     src = {"rmsnorm_adaln": "rmsnorm_adaln.cu", "qk_rmsnorm_rope": "qk_rmsnorm_rope.cu", "swiglu": "swiglu.cu"}
@@ -567,7 +573,7 @@ def run_tfk(args, ranks: Ranks) -> dict | None:
     if not args.no_valid_only:
         vo = ValidOnly(tfk, synth.get("valid_only"), device)
         k_vo = max(1, min(K, 200))
-        vms, vper, _, _ = time_steps(vo, k_vo, W, ranks)
+        vms, vper, _, _, _ = time_steps(vo, k_vo, W, ranks)
         vmax = ranks.max(vms / 1e3)
         valid = {"workload": f"valid_only: {vo.N} padded rows, {vo.L} valid, hidden {vo.wl.hidden}",
                  "valid_tokens_per_s": aggregate(vo.L * k_vo, ranks.world, vmax), "steps": k_vo,
@@ -683,7 +689,7 @@ def run_sweep(args, ranks: Ranks):
                 units.insert(5, Single("ulysses_unpack_p8", 4 * wl.n_heads * wl.head_dim * wl.rows,
                                        lambda: tfk.tfk_ulysses_unpack(send_q, wl.n_heads, wl.head_dim, P, dst=ch.out["q"])))
         for u in units:
-            total, per, _, _ = time_steps(u, K, W, ranks)
+            total, per, _, _, _ = time_steps(u, K, W, ranks)
             gms = graph_ms(u, K)
             if len(u.kernels) == 1:
                 ms = per[0]

@@ -7,7 +7,19 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "kernels.h"  // TFK_PDL
+
 namespace tfk {
+
+// Programmatic dependent launch (sm_90 and later): wait until every earlier
+// grid on the stream has completed and its memory operations are visible to
+// this grid.  A no-op for a launch without the programmatic attribute.  Every
+// kernel calls it before its first global memory access.
+__device__ __forceinline__ void grid_dep_wait() {
+#if TFK_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
 
 // Eight bf16 values in one 16-byte vector.
 struct alignas(16) Vec8 {

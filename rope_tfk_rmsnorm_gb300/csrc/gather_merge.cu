@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kThreads) copy_zero_kernel(const Vec8* __restr
                                                              Vec8* __restrict__ dst, int64_t n_copy,
                                                              int64_t n_total) {
     const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
+    grid_dep_wait();
     for (int64_t base = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; base < n_total;
          base += step) {
         Vec8 v[kUnroll];
@@ -54,10 +55,8 @@ cudaError_t launch_copy_zero(const uint16_t* src, uint16_t* dst, int64_t n_copy,
     int64_t grid = (int64_t)per_sm * di.sm_count * 4;
     const int64_t need = (n_total + per_block - 1) / per_block;
     if (grid > need) grid = need;
-    copy_zero_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(reinterpret_cast<const Vec8*>(src),
-                                                              reinterpret_cast<Vec8*>(dst), n_copy,
-                                                              n_total);
-    return cudaGetLastError();
+    return launch_kernel(copy_zero_kernel, (unsigned)grid, kThreads, 0, stream,
+                         reinterpret_cast<const Vec8*>(src), reinterpret_cast<Vec8*>(dst), n_copy, n_total);
 }
 
 }  // namespace

@@ -88,4 +88,34 @@ int blocks_per_sm(const void* func, int threads, size_t smem_bytes);
 constexpr int kInflightPerSm = TFK_INFLIGHT_KB * 1024;
 int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes);
 
+// Programmatic dependent launch: a kernel of this library may be scheduled
+// while the previous kernel on its stream drains its last CTAs.  Each kernel
+// runs only setup that touches no global memory before `grid_dep_wait()`
+// (common.cuh), which returns once every earlier grid of the stream has
+// completed and its memory operations are visible, so stream order holds for
+// any predecessor; the launch, CTA placement and that setup overlap the
+// predecessor's tail.  No kernel triggers its dependents early (no
+// `griddepcontrol.launch_dependents`): the implicit trigger at CTA exit
+// measured best.  With an early trigger the next kernel's waiting CTAs took
+// SM slots while this one still ran (per-frame chain 10% slower).
+#ifndef TFK_PDL
+#define TFK_PDL 1
+#endif
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                          cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = TFK_PDL ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return err != cudaSuccess ? err : cudaGetLastError();
+}
+
 }  // namespace tfk

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     // the lanes of a warp then read consecutive 16-byte pairs, no bank conflicts).
     for (int i = tid; i < half; i += nt) ftab[i] = tab.f[i];
     __syncthreads();
+    grid_dep_wait();
 
     const int lane = tid % G;
     const int group = hchunk * (nt / G) + tid / G;
@@ -324,8 +325,8 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
         last_theta = a.theta;
         last_dim = a.head_dim;
     }
-    qk_rope_kernel<HPT><<<(unsigned)grid, lay.threads, smem, stream>>>(a, lay, (int)want, stages, table);
-    return cudaGetLastError();
+    return launch_kernel(qk_rope_kernel<HPT>, (unsigned)grid, lay.threads, smem, stream, a, lay, (int)want, stages,
+                         table);
 }
 
 }  // namespace

@@ -79,6 +79,7 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Vec8* ring = reinterpret_cast<Vec8*>(smem_raw);  // [stages][nvec]
     __shared__ float partial[2][32];
+    grid_dep_wait();
 
     const int nvec = a.hidden >> 3;
     const int tid = threadIdx.x;
@@ -264,8 +265,7 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     }
     if (grid > work) grid = work;
     if (grid < 1) return cudaSuccess;
-    rmsnorm_adaln_kernel<V><<<(unsigned)grid, threads, smem, stream>>>(a, stages);
-    return cudaGetLastError();
+    return launch_kernel(rmsnorm_adaln_kernel<V>, (unsigned)grid, threads, smem, stream, a, stages);
 }
 
 }  // namespace

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const uint16_t* __rest
                                                           int64_t out_stride, int ffn,
                                                           int chunks_per_row, int64_t n_blocks) {
     const int nvec = ffn >> 3;
+    grid_dep_wait();
     for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
         const int64_t r = b / chunks_per_row;
         const int chunk = (int)(b - r * chunks_per_row);
@@ -72,9 +73,8 @@ cudaError_t launch_swiglu(const uint16_t* gate_up, int64_t in_stride, uint16_t* 
     // enough CTAs for several full waves; the loop covers the rest
     int64_t grid = (int64_t)per_sm * di.sm_count * 64;
     if (grid > n_blocks) grid = n_blocks;
-    swiglu_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(gate_up, in_stride, out, out_stride, ffn,
-                                                            chunks, n_blocks);
-    return cudaGetLastError();
+    return launch_kernel(swiglu_kernel, (unsigned)grid, kThreads, 0, stream, gate_up, in_stride, out,
+                         out_stride, ffn, chunks, n_blocks);
 }
 
 }  // namespace tfk

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kThreads) relayout_kernel(const uint16_t* __re
     const int64_t group_elems = rows * grp_row;
     const int64_t r0 = rows * (int64_t)blockIdx.x / gridDim.x;
     const int64_t r1 = rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
+    grid_dep_wait();
     for (int v = threadIdx.x; v < vec_per_row; v += kThreads) {
         const int h = v / vec_per_head;
         const int e = v - h * vec_per_head;
@@ -68,9 +69,8 @@ cudaError_t launch_ulysses_relayout(const uint16_t* src, uint16_t* dst, int64_t 
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)per_sm * di.sm_count;
     if (grid > rows) grid = rows;
-    relayout_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(src, dst, row_stride, rows, n_heads, head_dim,
-                                                             n_heads / groups, pack ? 1 : 0);
-    return cudaGetLastError();
+    return launch_kernel(relayout_kernel, (unsigned)grid, kThreads, 0, stream, src, dst, row_stride, rows,
+                         n_heads, head_dim, n_heads / groups, pack ? 1 : 0);
 }
 
 }  // namespace tfk

@@ -127,3 +127,78 @@ def test_a_failed_call_leaves_the_next_launch_unaffected(cuda):
         tfk.tfk_swiglu(d["gate_up"], ffn=12)          # rejected on the host
     for a, b in zip(_bits(_chain(wl, p, d)), ref):
         assert np.array_equal(a, b)
+
+
+def _dependent_steps(wl, p, d, buf, iters, sync_each=False):
+    """Each call reads what the call before it wrote (and the last one writes the
+    next iteration's input), so every launch has a read-after-write and a
+    write-after-read hazard on its predecessor: x -> RMSNorm+AdaLN -> y -> Q/K
+    norm+RoPE (q = k = y) -> z -> Ulysses pack and unpack of z's q half ->
+    SwiGLU(z) -> o -> RMSNorm+AdaLN in place on o -> gather of the valid rows ->
+    zero-tail merge back into x."""
+    x, y, z, o, c, s = buf["x"], buf["y"], buf["z"], buf["o"], buf["c"], buf["s"]
+    hd, H, D = wl.hidden, wl.n_heads, wl.head_dim
+
+    def done():
+        if sync_each:
+            torch.cuda.synchronize()
+
+    for _ in range(iters):
+        tfk.tfk_rmsnorm_adaln_indexed(x, p["w"], p["shift"], p["scale"], d["idx"], wl.eps, out=y); done()
+        tfk.tfk_qk_rmsnorm_rope_neox(y, y, p["w_q"], p["w_k"], d["pos"], H, D, wl.theta, wl.eps,
+                                     q_out=z[:, :hd], k_out=z[:, hd:]); done()
+        tfk.tfk_ulysses_pack(z[:, :hd], H, D, 4, dst=s); done()
+        tfk.tfk_ulysses_unpack(s, H, D, 4, dst=z[:, :hd]); done()
+        tfk.tfk_swiglu(z, out=o); done()
+        tfk.tfk_rmsnorm_adaln_indexed(o, p["w"], p["shift"], p["scale"], d["idx"], wl.eps, out=o); done()
+        tfk.tfk_valid_gather(o, c.shape[0], compact=c); done()
+        tfk.tfk_zero_tail_merge(c, x); done()
+
+
+def test_back_to_back_dependent_launches_keep_stream_order(cuda):
+    """The kernels may be scheduled while their predecessor on the stream drains
+    (programmatic dependent launch) and must still see all of its writes and
+    finish their reads before their successor writes: a chain of dependent
+    calls launched back to back, eagerly and from a CUDA graph, equals the same
+    chain with a device synchronisation after every call, bit for bit."""
+    wl, p, d = _problem(rows=4000, name="dep")
+    T, hd = wl.rows, wl.hidden
+
+    def buffers():
+        return {"x": d["x"].clone(), "y": torch.empty_like(d["x"]),
+                "z": torch.empty((T, 2 * hd), dtype=torch.bfloat16, device=cuda),
+                "o": torch.empty_like(d["x"]), "c": torch.empty((T - 123, hd), dtype=torch.bfloat16, device=cuda),
+                "s": torch.empty(T * hd, dtype=torch.bfloat16, device=cuda)}
+
+    iters = 12
+    ref = buffers()
+    _dependent_steps(wl, p, d, ref, iters, sync_each=True)
+    want = to_host(ref["x"])
+    assert np.isfinite(synth_f32(want)).all()
+    assert np.any(want != to_host(d["x"]))
+
+    eager = buffers()
+    _dependent_steps(wl, p, d, eager, iters)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(eager["x"]), want)
+
+    graphed = buffers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _dependent_steps(wl, p, d, buffers(), 1)   # warm the library's caches outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _dependent_steps(wl, p, d, graphed, iters)
+    for _ in range(2):
+        graphed["x"].copy_(d["x"])
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(to_host(graphed["x"]), want)
+
+
+def synth_f32(bits: np.ndarray) -> np.ndarray:
+    """Raw bf16 bits -> float32 values."""
+    return (bits.astype(np.uint32) << 16).view(np.float32)
