@@ -394,7 +394,7 @@ def cpu_baseline(wl, seconds: float) -> dict:
     return {"value": done / spent, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{done} rows of the {wl.name} workload ({wl.rows} rows) in chunks of {chunk}, "
                       f"{spent:.1f} s of timed fp64 oracle work (RMSNorm+AdaLN, Q/K RMSNorm+RoPE, SwiGLU, "
-                      f"bf16 rounding); input generation untimed",
+                      f"bf16 rounding, which the oracle runs on one thread); input generation untimed",
             "value_1thread": one / one_s, "sample_1thread": f"the first {one} rows on 1 thread"}
 
 
@@ -465,7 +465,7 @@ def _smi_id(device: torch.device) -> str:
         return ids[device.index] if device.index < len(ids) else str(device.index)
 
 
-def run_e2e(chain: Chain, steps: int, ranks: Ranks, chunks: int = 8) -> dict:
+def run_e2e(chain: Chain, steps: int, ranks: Ranks, chunks: int = 16) -> dict:
     """The same chain through the public API with host buffers.  Every step copies all
     of its inputs from pinned host memory and reads all of its outputs back; the rows
     are cut into `chunks` pieces so that the host-to-device copy of one piece, the
