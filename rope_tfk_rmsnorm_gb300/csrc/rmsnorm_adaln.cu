@@ -114,10 +114,13 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
             cp_async_commit();
         }
 
+        // The first row's modulation is fetched while the prologue rows are in
+        // flight, not after the first row has arrived.
         float mul[V][8], add[V][8];
         float mul2[1][8], add2[1][8];  // second cached row (used when V == 1)
-        int m_cur = -1, m_alt = -1;
-        int m_next = __ldg(a.mod_idx + r0);
+        int m_cur = __ldg(a.mod_idx + r0), m_alt = -1;
+        load_mod_row<V>(a, m_cur, col, ok, mul, add);
+        int m_next = m_cur;
         int stage_rd = 0, stage_wr = stages - 1;
 
         for (int it = 0; it < nrows; ++it) {
