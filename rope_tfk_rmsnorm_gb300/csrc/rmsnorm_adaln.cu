@@ -10,9 +10,9 @@
 // - Each thread owns the same 8*V columns of every row.  The norm weight for
 //   those columns lives in registers for the whole kernel, and the shift and
 //   (1 + scale) of the current modulation row are cached in registers and
-//   re-read only when mod_idx changes (two cached rows when V == 1, so a
-//   per-token choice between two rows costs no reload).  In steady state the
-//   fp32 parameters cost no memory traffic at all.
+//   re-read only when mod_idx changes (two cached rows when V == 1, i.e.
+//   hidden < 512, so a per-token choice between two rows costs no reload).
+//   In steady state the fp32 parameters cost no memory traffic at all.
 // - Activation rows are staged through a shared-memory ring with cp.async
 //   (16 B per thread, L1 bypassed), `stages - 1` rows ahead, so many rows are
 //   in flight per SM without holding them in registers.  A thread only reads
@@ -69,10 +69,10 @@ __device__ __forceinline__ void load_mod_row(const AdalnArgs& a, int m, const in
     }
 }
 
-// One or two vectors per thread (hidden <= 8192) run at least two CTAs per
+// One or two vectors per thread (hidden < 4096) run at least two CTAs per
 // SM, so that their per-row reductions and barriers overlap: one vector per
-// thread (at most 384 threads, two cached modulation rows) within 85
-// registers, two vectors within 64; wider rows get the full register file.
+// thread (two cached modulation rows) within 85 registers, two vectors within
+// 64; wider rows get the full register file.
 template <int V>
 __global__ void __launch_bounds__(V == 1 ? kMaxThreadsV1 : kMaxThreads, V <= 2 ? 2 : 1)
 rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
@@ -221,21 +221,27 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     }
 }
 
-// One vector per thread only for short rows (hidden < 2048, at most 256
-// threads): from 2048 on, two vectors per thread halve the CTA and let four
-// or five 64-register CTAs share an SM, which hides the per-row reduction
-// latency better than two big CTAs with the second cached modulation row.
-// From hidden 4096 on, four vectors per thread (128-160 threads, a barrier
-// over 4-5 warps): measured +2% at hidden 4096 and 5120 over two vectors.
+// Two vectors per thread from hidden 512 on, four from 4096 (128-160
+// threads, a barrier over 4-5 warps: +2% at hidden 4096 and 5120 over two),
+// eight beyond 16384.  Short rows are issue-bound rather than memory-bound:
+// the per-row loop, ring wait, two shuffle reductions and barrier are paid
+// for 8 elements per thread with one vector.  Two vectors per thread instead
+// of one measured 58% -> 79-83% of the copy bandwidth at hidden 512-1536
+// (constant index; 54% -> 66-68% with a per-token coin flip, despite losing
+// the second cached modulation row), and let four or more 64-register CTAs
+// share an SM.  One vector per thread is left for hidden < 512.
 #ifndef TFK_A1_MIN_V
 #define TFK_A1_MIN_V 2
+#endif
+#ifndef TFK_A1_V2_FROM_NVEC
+#define TFK_A1_V2_FROM_NVEC 64
 #endif
 #ifndef TFK_A1_V4_FROM_NVEC
 #define TFK_A1_V4_FROM_NVEC 512
 #endif
 bool choose_shape(int hidden, int* v, int* threads) {
     const int nvec = hidden / 8;
-    const int first = nvec >= TFK_A1_V4_FROM_NVEC ? 4 : (nvec >= 256 ? TFK_A1_MIN_V : 1);
+    const int first = nvec >= TFK_A1_V4_FROM_NVEC ? 4 : (nvec >= TFK_A1_V2_FROM_NVEC ? TFK_A1_MIN_V : 1);
     for (int cand = first; cand <= 8; cand *= 2) {
         const int t = (nvec + cand - 1) / cand;
         if (t <= (cand == 1 ? kMaxThreadsV1 : kMaxThreads)) {
