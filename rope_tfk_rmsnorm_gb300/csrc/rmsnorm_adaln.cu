@@ -229,7 +229,11 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
 // of one measured 58% -> 79-83% of the copy bandwidth at hidden 512-1536
 // (constant index; 54% -> 66-68% with a per-token coin flip, despite losing
 // the second cached modulation row), and let four or more 64-register CTAs
-// share an SM.  One vector per thread is left for hidden < 512.
+// share an SM.  One vector per thread is left for hidden < 512.  Hidden
+// 6144-8192 goes back to two vectors: four would take ~120 registers for
+// 192-256 threads, i.e. two CTAs of 6-8 warps per SM (measured 74% -> 78% at
+// 6144, +1% at 8192; at 4096 and 5120 four vectors stay ahead).  Beyond
+// 16384 eight vectors do not fit in 128 registers and spill (~40-47%).
 #ifndef TFK_A1_MIN_V
 #define TFK_A1_MIN_V 2
 #endif
@@ -241,7 +245,8 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
 #endif
 bool choose_shape(int hidden, int* v, int* threads) {
     const int nvec = hidden / 8;
-    const int first = nvec >= TFK_A1_V4_FROM_NVEC ? 4 : (nvec >= TFK_A1_V2_FROM_NVEC ? TFK_A1_MIN_V : 1);
+    int first = nvec >= TFK_A1_V4_FROM_NVEC ? 4 : (nvec >= TFK_A1_V2_FROM_NVEC ? TFK_A1_MIN_V : 1);
+    if (nvec >= 768 && nvec <= 1024) first = 2;  // hidden 6144-8192: 384-512 threads of 64 registers
     for (int cand = first; cand <= 8; cand *= 2) {
         const int t = (nvec + cand - 1) / cand;
         if (t <= (cand == 1 ? kMaxThreadsV1 : kMaxThreads)) {

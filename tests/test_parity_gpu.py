@@ -130,6 +130,9 @@ ADALN_CASES = [
     (300, 3072, 4, "pairs"),         # two rows alternate per token, then two others
     (129, 5120, 2, "blocks"),
     (1000, 4104, 6, "random"),       # 513 vectors: ragged last thread of a 2-vector layout
+    (200, 6144, 3, "random"),        # 6144-8192: two vectors per thread, 384-512 threads
+    (150, 8192, 2, "pairs"),
+    (90, 8200, 3, "random"),         # 1025 vectors: back to four per thread, ragged
     (64, 16384, 3, "random"),
     (17, 32768, 2, "random"),        # largest hidden
     (2500, 512, 28, "blocks"),
