@@ -290,7 +290,10 @@ def test_qk_position_zero_is_plain_head_rmsnorm(cuda):
 # SwiGLU
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("rows,ffn", [(1, 8), (5, 104), (300, 1024), (37, 13824), (3, 8200)])
+@pytest.mark.parametrize("rows,ffn", [(1, 8), (5, 104), (300, 1024), (37, 13824), (3, 8200),
+                                      (1001, 3072),    # 2 whole rows per block, odd row count
+                                      (777, 520),      # 15 rows of 65 vectors per block, 49 slots idle
+                                      (70, 4096), (70, 4104)])  # the last width with 2 rows per block, and the first without
 def test_swiglu_ragged(cuda, rows, ffn):
     rng = np.random.default_rng(rows * 31 + ffn)
     gu = rand_bits(rng, (rows, 2 * ffn), 4.0)
