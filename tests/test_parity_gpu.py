@@ -597,7 +597,10 @@ def test_qk_ulysses_send_layout(cuda, rows, H, D, P):
 
 
 @pytest.mark.parametrize("rows,H,D,P,stride_pad", [(1, 1, 8, 1, 0), (100, 24, 128, 4, 0), (77, 40, 128, 8, 64),
-                                                   (5, 6, 40, 3, 8)])
+                                                   (5, 6, 40, 3, 8),
+                                                   (1003, 24, 128, 4, 0),   # many 4-row tiles, ragged last tile
+                                                   (203, 64, 128, 8, 0),    # 8192 values per row: 4 vectors per thread
+                                                   (37, 72, 128, 8, 16)])   # 9216 values: the column-walking kernel
 def test_ulysses_pack_unpack_bit_exact(cuda, rows, H, D, P, stride_pad):
     rng = np.random.default_rng(rows * H + P)
     x = rng.integers(0, 65536, (rows, H * D), dtype=np.uint32).astype(np.uint16)
