@@ -73,8 +73,19 @@ __device__ __forceinline__ void load_mod_row(const AdalnArgs& a, int m, const in
 // SM, so that their per-row reductions and barriers overlap: one vector per
 // thread (two cached modulation rows) within 85 registers, two vectors within
 // 64; wider rows get the full register file.
-template <int V>
-__global__ void __launch_bounds__(V == 1 ? kMaxThreadsV1 : kMaxThreads, V <= 2 ? 2 : 1)
+// MAXT: most threads per CTA of this instantiation.  kExact: every thread
+// owns V whole vectors (8 * V * threads == hidden: hidden a multiple of 512
+// for V = 2, of 1024 for V = 4), so no bounds predicates.  Two vectors in at
+// most 256 threads get 80 registers when exact: with 64 the compiler re-read
+// thread indices and kernel parameters inside the row loop.  Measured
+// against 64 registers with predicates: +7 points at hidden 2048, +3 at
+// 3072 x 8192 rows, even at 3072 x 30358; four exact vectors +1.5 points at
+// 4096 and 5120.
+template <int V, int MAXT, bool kExact>
+constexpr int kMinBlocks = V == 1 ? 2 : (V == 2 ? (MAXT <= 256 && kExact ? 3 : 2 * (512 / MAXT)) : 1);
+
+template <int V, int MAXT, bool kExact>
+__global__ void __launch_bounds__(MAXT, (kMinBlocks<V, MAXT, kExact>))
 rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Vec8* ring = reinterpret_cast<Vec8*>(smem_raw);  // [stages][nvec]
@@ -98,7 +109,7 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
 #pragma unroll
     for (int i = 0; i < V; ++i) {
         col[i] = tid + i * nt;
-        ok[i] = col[i] < nvec;
+        ok[i] = kExact || col[i] < nvec;
     }
 
     if (nrows > 0) {  // uniform over the CTA
@@ -258,13 +269,13 @@ bool choose_shape(int hidden, int* v, int* threads) {
     return false;
 }
 
-template <int V>
+template <int V, int MAXT, bool kExact>
 cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
     const int row_bytes = (a.hidden / 8) * 16;
-    const void* fn = reinterpret_cast<const void*>(&rmsnorm_adaln_kernel<V>);
+    const void* fn = reinterpret_cast<const void*>(&rmsnorm_adaln_kernel<V, MAXT, kExact>);
     const int by_regs = blocks_per_sm(fn, threads, 0);
     if (by_regs <= 0) return cudaErrorInvalidConfiguration;
     const int stages = pick_stages(by_regs, row_bytes, 0);
@@ -279,7 +290,7 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     }
     if (grid > work) grid = work;
     if (grid < 1) return cudaSuccess;
-    return launch_kernel(rmsnorm_adaln_kernel<V>, (unsigned)grid, threads, smem, stream, a, stages);
+    return launch_kernel(rmsnorm_adaln_kernel<V, MAXT, kExact>, (unsigned)grid, threads, smem, stream, a, stages);
 }
 
 }  // namespace
@@ -292,11 +303,17 @@ bool rmsnorm_adaln_supported(int hidden) {
 cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, cudaStream_t stream) {
     int v = 0, threads = 0;
     if (!choose_shape(a.hidden, &v, &threads)) return cudaErrorInvalidValue;
+    const bool exact = 8 * v * threads == a.hidden;
     switch (v) {
-        case 1: return launch_v<1>(a, threads, stream);
-        case 2: return launch_v<2>(a, threads, stream);
-        case 4: return launch_v<4>(a, threads, stream);
-        default: return launch_v<8>(a, threads, stream);
+        case 1: return launch_v<1, kMaxThreadsV1, false>(a, threads, stream);
+        case 2:
+            if (threads <= 256)
+                return exact ? launch_v<2, 256, true>(a, threads, stream) : launch_v<2, 256, false>(a, threads, stream);
+            return launch_v<2, kMaxThreads, false>(a, threads, stream);
+        case 4:
+            return exact ? launch_v<4, kMaxThreads, true>(a, threads, stream)
+                         : launch_v<4, kMaxThreads, false>(a, threads, stream);
+        default: return launch_v<8, kMaxThreads, false>(a, threads, stream);
     }
 }
 
