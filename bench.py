@@ -56,6 +56,8 @@ def parse_args(argv=None):
                     help="use only the first ROWS tokens of the workload (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="time box of the oracle baseline")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="time budget of the whole --impl reference run (oracle steps are sized to it)")
     ap.add_argument("--no-valid-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -407,7 +409,7 @@ def run_reference(args, ranks: Ranks) -> dict | None:
     threads = os.cpu_count() or 1
     p = synth.params(wl)
     oracle.build()
-    budget = 120.0 / max(1, args.steps + args.warmup)      # seconds per step: the run ends in minutes
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)  # seconds per step: the run ends in minutes
     rows_per_step = 64
     probe = _oracle_chain(oracle, wl, np.arange(rows_per_step), p, threads)
     rows_per_step = int(max(16, min(4096, rows_per_step * budget / max(probe, 1e-6))))
