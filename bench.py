@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-valid-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep-workloads", default="tiny,medium,valid_only,large,per_frame",
+                    help="comma-separated workloads of --sweep (--rows cuts the chain workloads to a prefix)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every kernel on every workload (one JSON line per workload) instead of the step")
     return ap.parse_args(argv)
@@ -646,8 +648,8 @@ def run_sweep(args, ranks: Ranks):
     torch.cuda.set_device(device)
     peak = measured_peaks()["hbm_gbs"]
     K, W = max(1, min(args.steps, 100)), max(3, args.warmup)
-    for name in ("tiny", "medium", "valid_only", "large", "per_frame"):
-        wl = synth.get(name)
+    for name in [w.strip() for w in args.sweep_workloads.split(",") if w.strip()]:
+        wl = synth.get(name) if name == "valid_only" else prefix(synth.get(name), args.rows)
         res = {}
         if name == "valid_only":
             vo = ValidOnly(tfk, wl, device)
@@ -691,8 +693,9 @@ def run_sweep(args, ranks: Ranks):
                 units.insert(5, Single("ulysses_unpack_p8", 4 * wl.n_heads * wl.head_dim * wl.rows,
                                        lambda: tfk.tfk_ulysses_unpack(send_q, wl.n_heads, wl.head_dim, P, dst=ch.out["q"])))
         for u in units:
-            total, per, _, _, _ = time_steps(u, K, W, ranks)
-            gms = graph_ms(u, K)
+            with torch.cuda.nvtx.range(u.kernels[0] if len(u.kernels) == 1 else "chain"):  # ncu --nvtx-include
+                total, per, _, _, _ = time_steps(u, K, W, ranks)
+                gms = graph_ms(u, K)
             if len(u.kernels) == 1:
                 ms = per[0]
                 rows = rows_for.get(u.kernels[0], wl.rows)
