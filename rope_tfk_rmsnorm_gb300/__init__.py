@@ -61,6 +61,8 @@ class TfkError(RuntimeError):
 def load() -> ctypes.CDLL:
     """Load libtfk.so (built by ``__graft_entry__.build()`` or ``build.py``); raises if absent."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -79,16 +81,16 @@ def _check(status: int):
         raise TfkError(status, load().tfk_last_error_message().decode())
 
 
-def _stream(t: torch.Tensor, stream) -> ctypes.c_void_p:
+def _stream(t: torch.Tensor, stream) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream(t.device)
+        return torch.cuda.current_stream(t.device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
-        stream = stream.cuda_stream
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
-def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
-    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+def _ptr(t: torch.Tensor | None) -> int:
+    return 0 if t is None else t.data_ptr()
 
 
 def _rows(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> int:
