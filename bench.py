@@ -49,7 +49,7 @@ def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["tfk", "reference"], default="tfk")
     ap.add_argument("--workload", default="large", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--rows", type=int, default=0,
@@ -365,7 +365,8 @@ def time_steps(work, steps: int, warmup: int, ranks: Ranks):
 
 def _oracle_chain(oracle, wl, rows: np.ndarray, p: dict, threads: int):
     """Generate (untimed) and run (timed) the oracle chain on the given rows; returns seconds."""
-    x, q, k, gu = (synth.activation(wl, t, rows=rows) for t in ("x", "q", "k", "gate_up"))
+    x, q, k = (synth.activation(wl, t, rows=rows) for t in ("x", "q", "k"))
+    gu = synth.activation(wl, "gate_up", rows=rows) if wl.ffn > 0 else None   # no FFN on the valid-only workload
     idx, pos = synth.mod_index(wl, rows), synth.positions(wl, rows)
     t0 = time.perf_counter()
     oracle.round_bf16(oracle.rmsnorm_adaln_indexed(x, p["w"], p["shift"], p["scale"], idx, wl.eps, threads=threads))
@@ -373,8 +374,23 @@ def _oracle_chain(oracle, wl, rows: np.ndarray, p: dict, threads: int):
                                          wl.eps, threads=threads)
     oracle.round_bf16(qo)
     oracle.round_bf16(ko)
-    oracle.round_bf16(oracle.swiglu(gu, threads=threads))
+    if gu is not None:
+        oracle.round_bf16(oracle.swiglu(gu, threads=threads))
     return time.perf_counter() - t0
+
+
+def oracle_rates(wl) -> dict:
+    """The oracle beside every sweep workload: a bounded sample of rows on one thread
+    and on all host threads (a second or two of CPU work per workload)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    p = synth.params(wl)
+    limit = synth.valid_len(wl)
+    n1, nall = min(limit, 32), min(limit, 512)
+    t1 = _oracle_chain(oracle, wl, np.arange(n1), p, 1)
+    tall = _oracle_chain(oracle, wl, np.arange(nall), p, threads)
+    return {"tokens_per_s_1thread": n1 / t1, "tokens_per_s_all_threads": nall / tall, "threads": threads,
+            "sample": f"first {n1} / {nall} rows, fp64 oracle chain, input generation untimed"}
 
 
 def cpu_baseline(wl, seconds: float) -> dict:
@@ -648,6 +664,8 @@ def run_sweep(args, ranks: Ranks):
     torch.cuda.set_device(device)
     peak = measured_peaks()["hbm_gbs"]
     K, W = max(1, min(args.steps, 100)), max(3, args.warmup)
+    import oracle
+    oracle.build()
     for name in [w.strip() for w in args.sweep_workloads.split(",") if w.strip()]:
         wl = synth.get(name) if name == "valid_only" else prefix(synth.get(name), args.rows)
         res = {}
@@ -709,7 +727,7 @@ def run_sweep(args, ranks: Ranks):
                     graph_ms=gms, graph_frac=_roof(sum(u.bytes), gms, peak)["frac"], kernels=u.kernels)
         if ranks.rank == 0:
             print(json.dumps({"sweep": name, "workload": workload_config(wl)["workload"], "steps": K,
-                              "peak_gbs": peak, "results": res}), flush=True)
+                              "peak_gbs": peak, "results": res, "oracle": oracle_rates(wl)}), flush=True)
         del units
         torch.cuda.empty_cache()
 
