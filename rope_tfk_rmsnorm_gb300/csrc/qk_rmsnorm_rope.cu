@@ -322,6 +322,7 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
         const int64_t chunks = (work + kRowsPerCta - 1) / (kRowsPerCta > 0 ? kRowsPerCta : 1);
         if (chunks > want) want = chunks;
     }
+    if (want > (1 << 24)) want = 1 << 24;  // the token split covers any count; keeps rows * chunk in range
     if (want > work) want = work;
     if (want < 1) return cudaSuccess;
     const int64_t grid = want * lay.head_chunks;

@@ -288,6 +288,7 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
         const int64_t chunks = (work + kRowsPerCta - 1) / (kRowsPerCta > 0 ? kRowsPerCta : 1);
         if (chunks > grid && work >= kChunkMinRun * grid) grid = chunks;
     }
+    if (grid > (1 << 24)) grid = 1 << 24;  // the row split covers any grid; keeps rows * blockIdx in range
     if (grid > work) grid = work;
     if (grid < 1) return cudaSuccess;
     return launch_kernel(rmsnorm_adaln_kernel<V, MAXT, kExact>, (unsigned)grid, threads, smem, stream, a, stages);

@@ -137,6 +137,7 @@ cudaError_t launch_ulysses_relayout(const uint16_t* src, uint16_t* dst, int64_t 
     int64_t grid = (int64_t)per_sm * di.sm_count;
     const int64_t tiles = (rows + kRowsPerCta - 1) / kRowsPerCta;
     if (tiles > grid) grid = tiles;
+    if (grid > (1 << 24)) grid = 1 << 24;  // the row split covers any grid; keeps rows * blockIdx in range
     if (grid > rows) grid = rows;
     return launch_kernel(k, (unsigned)grid, kThreads, 0, stream, src, dst, row_stride, rows,
                          n_heads, head_dim, n_heads / groups, pack ? 1 : 0);
