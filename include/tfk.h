@@ -71,9 +71,9 @@ const char* tfk_last_error_message(void);
 tfk_status tfk_debug_fail_next_launch(int32_t cuda_error);
 
 /*
- * RMSNorm fused with indexed AdaLN modulation ("Fuse RMSNorm with indexed
- * AdaLN modulation", TeleFuser PR #38 section 2; "indexed modulation",
- * TeleFuser PR #23 "Changes Made").  For every row t, with m = mod_idx[t]:
+ * RMSNorm fused with indexed AdaLN modulation (TeleFuser PR #38, section 2,
+ * the RMSNorm + indexed AdaLN fusion; TeleFuser PR #23, section Changes Made,
+ * the indexed-modulation kernel).  For every row t, with m = mod_idx[t]:
  *
  *   inv_rms = 1 / sqrt( (1/hidden) * sum_j x[t,j]^2 + eps )
  *   y[t,j]  = bf16( x[t,j] * inv_rms * weight[j] * (1 + scale[m,j]) + shift[m,j] )
@@ -93,9 +93,9 @@ tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride,
                                      int64_t rows, int32_t hidden, float eps, void* stream);
 
 /*
- * Q/K per-head RMSNorm fused with NeoX rotate-half RoPE ("Fuse Q/K RMSNorm,
- * RoPE, and Ulysses packing", TeleFuser PR #38 section 2; "Q/K normalization
- * plus NeoX RoPE", TeleFuser PR #23 "Changes Made").  For q (with q_weight)
+ * Q/K per-head RMSNorm fused with NeoX rotate-half RoPE (TeleFuser PR #38,
+ * section 2, the Q/K norm + RoPE fusion; TeleFuser PR #23, section Changes
+ * Made, the Q/K normalization with NeoX RoPE kernel).  For q (with q_weight)
  * and for k (with k_weight), every row t and head h, with D = head_dim:
  *
  *   n[d]       = v[t,h,d] / sqrt( (1/D) * sum_d v[t,h,d]^2 + eps ) * w[d]
@@ -123,9 +123,9 @@ tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_
                                     float theta, float eps, void* stream);
 
 /*
- * Fixed-valid mode of the two normalisation kernels ("Add fixed-valid and
- * valid-only attention modes" and "Fuse valid-only gather with zero-tail
- * merge", TeleFuser PR #38 section 2): the kernel works directly on the padded
+ * Fixed-valid mode of the two normalisation kernels (TeleFuser PR #38,
+ * section 2: the fixed-valid and valid-only modes, and the gather / zero-tail
+ * merge they make unnecessary): the kernel works directly on the padded
  * token buffer.  Rows [0, valid_rows) are computed exactly as by the entry
  * points above (reading only those rows of the inputs, mod_idx and
  * positions); rows [valid_rows, padded_rows) of the outputs are written +0.0
@@ -155,8 +155,8 @@ tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf1
                                                 void* stream);
 
 /*
- * Q/K RMSNorm + NeoX RoPE fused with Ulysses packing ("Fuse Q/K RMSNorm, RoPE,
- * and Ulysses packing", TeleFuser PR #38 section 2): the same arithmetic as
+ * Q/K RMSNorm + NeoX RoPE fused with Ulysses packing (TeleFuser PR #38,
+ * section 2, the Q/K norm + RoPE fusion with the packing): the same arithmetic as
  * tfk_qk_rmsnorm_rope_neox, stored directly in the send layout of the
  * Ulysses sequence-parallel all-to-all of degree P = sp_degree:
  *
@@ -176,8 +176,8 @@ tfk_status tfk_qk_rmsnorm_rope_neox_ulysses(const tfk_bf16* q, const tfk_bf16* k
                                             float theta, float eps, void* stream);
 
 /*
- * Ulysses head <-> sequence relayout ("Ulysses relayout", TeleFuser PR #23
- * "Changes Made"), a bit-exact permutation around the all-to-all:
+ * Ulysses head <-> sequence relayout (TeleFuser PR #23, section Changes Made,
+ * the Ulysses relayout kernel), a bit-exact permutation around the all-to-all:
  *
  *   pack:    dst[p][t][j][d] = src[t][(p*H/P + j)*D + d]
  *   unpack:  dst[t][(p*H/P + j)*D + d] = src[p][t][j][d]
@@ -194,8 +194,8 @@ tfk_status tfk_ulysses_unpack(const tfk_bf16* src, tfk_bf16* dst, int64_t dst_ro
                               int32_t n_heads, int32_t head_dim, int32_t sp_degree, void* stream);
 
 /*
- * SwiGLU on the FFN up-projection output ("SwiGLU", TeleFuser PR #23
- * "Changes Made"):
+ * SwiGLU on the FFN up-projection output (TeleFuser PR #23, section Changes
+ * Made, the SwiGLU kernel):
  *
  *   out[t,j] = bf16( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),
  *   g = gate_up[t, j],  u = gate_up[t, ffn + j]       (0 <= j < ffn)
@@ -210,8 +210,8 @@ tfk_status tfk_swiglu(const tfk_bf16* gate_up, int64_t in_row_stride,
                       int64_t rows, int32_t ffn, void* stream);
 
 /*
- * Valid-only gather ("Fuse valid-only gather with zero-tail merge", TeleFuser
- * PR #38 section 2): copy the valid prefix of a padded token buffer into a
+ * Valid-only gather (TeleFuser PR #38, section 2, the gather fused with the
+ * zero-tail merge): copy the valid prefix of a padded token buffer into a
  * compact buffer, bit for bit.
  *
  *   compact[i, :] = padded[i, :]     for 0 <= i < valid_rows

@@ -260,8 +260,8 @@ def qk_rmsnorm_rope_neox_fixed_valid(q_padded, k_padded, valid_rows: int, q_weig
     return qo, ko
 
 
-# ---- Ulysses relayout ("Ulysses relayout", TeleFuser PR #23; packing fused into Q/K
-#      RMSNorm + RoPE, TeleFuser PR #38 section 2) ----
+# ---- Ulysses relayout (TeleFuser PR #23, section Changes Made; packing fused into
+#      Q/K RMSNorm + RoPE, TeleFuser PR #38, section 2) ----
 
 def ulysses_pack(rows_layout: np.ndarray, n_heads: int, head_dim: int, sp_degree: int) -> np.ndarray:
     """[rows, n_heads*head_dim] -> [sp_degree, rows, n_heads/sp_degree, head_dim]: block p holds the

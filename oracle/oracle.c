@@ -9,13 +9,13 @@
  * Source of the definitions: the TeleFuser pages on MiniMax H3 name the fused
  * ops and their order but print no formula, so each function states the
  * plain textbook definition it follows:
- *   - "Fuse RMSNorm with indexed AdaLN modulation" (TeleFuser PR #38, section 2
- *     "Lossless optimizations from PR #37"; PR #23 "Changes Made": fused
- *     kernels "for indexed modulation");
- *   - "Fuse Q/K RMSNorm, RoPE, and Ulysses packing" (PR #38, section 2) and
- *     "Q/K normalization plus NeoX RoPE" (PR #23, "Changes Made");
- *   - "SwiGLU" (PR #23, "Changes Made");
- *   - "Fuse valid-only gather with zero-tail merge" (PR #38, section 2).
+ *   - RMSNorm fused with the indexed AdaLN modulation (TeleFuser PR #38,
+ *     section 2 "Lossless optimizations from PR #37"; TeleFuser PR #23,
+ *     section Changes Made, its indexed-modulation kernel);
+ *   - Q/K RMSNorm followed by NeoX RoPE (PR #38, section 2; PR #23, section
+ *     Changes Made);
+ *   - SwiGLU (PR #23, section Changes Made);
+ *   - the valid-only gather and the zero-tail merge (PR #38, section 2).
  *
  * Arithmetic: bf16 and fp32 inputs are widened exactly to double; every
  * intermediate is a double; results are returned as doubles, and

@@ -1,5 +1,6 @@
-// gather_merge.cu - valid-only gather and zero-tail merge ("Fuse valid-only
-// gather with zero-tail merge", TeleFuser PR #38 section 2).
+// gather_merge.cu - valid-only gather and zero-tail merge (TeleFuser PR #38,
+// section 2: the gather of the valid rows fused with the merge that writes
+// them back and zeroes the tail).
 //
 // Both buffers have contiguous rows, so the valid prefix of L rows is one
 // contiguous run of L*hidden bf16 values: the gather is a bit-exact 16-byte

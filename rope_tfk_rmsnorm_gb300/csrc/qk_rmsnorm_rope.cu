@@ -5,8 +5,9 @@
 //   a_i        = pos[t] * theta^(-2i/D),  i < D/2
 //   out[i]     = n[i] cos a_i - n[i+D/2] sin a_i
 //   out[i+D/2] = n[i+D/2] cos a_i + n[i] sin a_i
-// ("Fuse Q/K RMSNorm, RoPE, and Ulysses packing", TeleFuser PR #38 section 2;
-// "Q/K normalization plus NeoX RoPE", TeleFuser PR #23 "Changes Made").
+// (TeleFuser PR #38, section 2: Q/K RMSNorm and RoPE fused, together with the
+// Ulysses packing; TeleFuser PR #23, section Changes Made: the Q/K
+// normalization with NeoX RoPE kernel.)
 //
 // Design (HBM-bound: 4 bytes per q/k element read + written, plus 4 B/token):
 // - A head is served by G lanes (G = D/16 rounded up to a power of two);
@@ -30,8 +31,8 @@
 //   hardware sin/cos approximations are accurate to about 4e-7 absolute, so
 //   no fp64 and no range reduction is needed per token.
 // - The output can go straight into the Ulysses all-to-all send layout
-//   [groups][rows][heads/groups][D] ("Fuse Q/K RMSNorm, RoPE, and Ulysses
-//   packing", TeleFuser PR #38 section 2): only the store address changes.
+//   [groups][rows][heads/groups][D] (the Ulysses packing fused into this step,
+//   TeleFuser PR #38, section 2): only the store address changes.
 #include <cmath>
 
 #include "common.cuh"

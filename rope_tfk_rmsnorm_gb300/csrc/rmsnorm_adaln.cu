@@ -1,8 +1,9 @@
 // rmsnorm_adaln.cu - RMSNorm fused with indexed AdaLN modulation.
 //
 // y[t,j] = bf16( x[t,j] * rsqrt(mean_j x[t,:]^2 + eps) * w[j] * (1 + scale[m,j]) + shift[m,j] ),
-// m = mod_idx[t]  ("Fuse RMSNorm with indexed AdaLN modulation", TeleFuser
-// PR #38 section 2; "indexed modulation", TeleFuser PR #23 "Changes Made").
+// m = mod_idx[t].  TeleFuser PR #38, section 2: RMSNorm fused with the
+// per-token indexed AdaLN modulation; TeleFuser PR #23, section Changes
+// Made: the indexed-modulation kernel.
 //
 // Design (HBM-bound: 2 bytes read + 2 bytes written per element):
 // - Persistent CTAs, each owning a contiguous run of rows, so the modulation

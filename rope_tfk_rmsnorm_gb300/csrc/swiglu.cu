@@ -1,5 +1,5 @@
-// swiglu.cu - SwiGLU on the FFN up-projection output ("SwiGLU", TeleFuser
-// PR #23 "Changes Made"):  out[t,j] = bf16( silu(g) * u ),
+// swiglu.cu - SwiGLU on the FFN up-projection output (TeleFuser PR #23,
+// section Changes Made, its SwiGLU kernel):  out[t,j] = bf16( silu(g) * u ),
 // silu(g) = g / (1 + exp(-g)),  g = gate_up[t,j],  u = gate_up[t,ffn+j].
 //
 // Design (HBM-bound: 4 bytes read + 2 written per output element): every CTA

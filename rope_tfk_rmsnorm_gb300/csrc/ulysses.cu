@@ -1,6 +1,6 @@
 // ulysses.cu - head <-> sequence relayout around the Ulysses all-to-all
-// ("Ulysses relayout", TeleFuser PR #23 "Changes Made"; "Fuse Q/K RMSNorm,
-// RoPE, and Ulysses packing", TeleFuser PR #38 section 2).
+// (TeleFuser PR #23, section Changes Made: the Ulysses relayout kernel;
+// TeleFuser PR #38, section 2: the packing fused into Q/K norm and RoPE).
 //
 // pack:   src [rows, row_stride] holding H heads of D values per row
 //         -> dst [G][rows][H/G][D]: block g is what sequence-parallel rank g
