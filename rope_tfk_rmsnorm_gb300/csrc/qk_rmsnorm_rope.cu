@@ -287,7 +287,12 @@ bool choose_layout(int n_heads, int head_dim, int heads_per_group, Layout* lay) 
     if (heads_per_group < 1 || n_heads % heads_per_group != 0) return false;
     int L = head_dim / 16, G = 1;
     while (G < L) G <<= 1;
-    const int hpt = n_heads >= 4 ? 4 : (n_heads >= 2 ? 2 : 1);
+    // 3 heads per group for 3, 6 and 9 heads, where groups of 4 would leave a
+    // quarter of their head slots masked (6 x 128: 88% -> 94%); elsewhere 4
+    // heads per group measured ahead even with idle lanes or masked heads
+    // (25 x 128: 95% with 4 against 86% with 3; 12 x 128 within 1%).
+    int hpt = n_heads >= 4 ? 4 : (n_heads >= 2 ? 2 : 1);
+    if (n_heads % 3 == 0 && n_heads % 4 != 0 && n_heads <= 9) hpt = 3;
     const int64_t groups = 2LL * ((n_heads + hpt - 1) / hpt);
     // as few head chunks as possible with at most kMaxThreads threads per CTA
     const int64_t per_cta = kMaxThreads / G;
@@ -355,6 +360,7 @@ cudaError_t launch_qk_rmsnorm_rope(const QkRopeArgs& a, cudaStream_t stream) {
     switch (lay.hpt) {
         case 1: return launch_h<1, false>(a, lay, stream);
         case 2: return masked ? launch_h<2, true>(a, lay, stream) : launch_h<2, false>(a, lay, stream);
+        case 3: return masked ? launch_h<3, true>(a, lay, stream) : launch_h<3, false>(a, lay, stream);
         default: return masked ? launch_h<4, true>(a, lay, stream) : launch_h<4, false>(a, lay, stream);
     }
 }

@@ -224,6 +224,8 @@ QK_CASES = [
     (19, 128, 128),    # 4 heads per lane group, several head chunks
     (13, 201, 128),    # odd head count: the last lane group of q and of k holds 1 head
     (23, 30, 96),      # 2 of 4 heads in the last group, 6 data lanes in a group of 8
+    (41, 6, 128),      # 3 heads per lane group
+    (19, 9, 64),
     (7, 300, 64),      # many heads: a 2-D grid of token runs x head chunks
     (11, 4, 256),
     (9, 2, 512),
@@ -580,7 +582,8 @@ def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
 @pytest.mark.parametrize("rows,H,D,P", [(50, 8, 128, 1), (50, 8, 128, 2), (129, 24, 128, 4), (33, 40, 128, 8),
                                         (17, 6, 64, 3),
                                         (21, 25, 128, 5),   # 4 heads per lane group, the last one masked,
-                                        (9, 30, 96, 3)])    # groups spanning two ranks' blocks
+                                        (9, 30, 96, 3),     # groups spanning two ranks' blocks
+                                        (15, 6, 128, 2), (11, 9, 64, 3)])  # 3 heads per lane group
 def test_qk_ulysses_send_layout(cuda, rows, H, D, P):
     rng = np.random.default_rng(rows + 100 * P)
     q = rand_bits(rng, (rows, H * D))
