@@ -96,9 +96,11 @@ struct Layout {
     int threads;      // per CTA
     int groups;       // lane groups in the whole problem: 2 * ceil(n_heads / hpt)
     int head_chunks;  // CTAs along the head dimension
+    int groups_per_cta;  // lane groups of one token stream of a CTA
+    int streams;      // token streams per CTA (side by side, each its own rows)
 };
 
-template <int HPT, bool kMasked>
+template <int HPT, bool kMasked, bool kStreams>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const QkRopeArgs a, const Layout lay,
                                                               const int token_chunks, const int stages,
                                                               const __grid_constant__ RopeTable tab) {
@@ -117,9 +119,19 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
 
     const int tchunk = blockIdx.x % token_chunks;
     const int hchunk = blockIdx.x / token_chunks;
-    const int64_t r0 = a.rows * (int64_t)tchunk / token_chunks;
-    const int64_t r1 = a.rows * (int64_t)(tchunk + 1) / token_chunks;
-    const int nrows = (int)(r1 - r0);
+    // A CTA may run several token streams side by side (to fill its warps when
+    // one stream's lane groups leave lanes idle); stream s takes part s of the
+    // CTA's token run.  Nothing below synchronises across groups: the only
+    // barrier is the table copy above, and each head's reduction is a shuffle
+    // within its own aligned G-lane group.
+    const int gi = tid / G;
+    const int nstreams = kStreams ? lay.streams : 1;
+    int sidx = 0;
+    if constexpr (kStreams) sidx = gi / lay.groups_per_cta < nstreams ? gi / lay.groups_per_cta : nstreams - 1;
+    const int64_t c0 = a.rows * (int64_t)tchunk / token_chunks;
+    const int64_t c1 = a.rows * (int64_t)(tchunk + 1) / token_chunks;
+    const int64_t r0 = kStreams ? c0 + (c1 - c0) * sidx / nstreams : c0;
+    const int nrows = (int)((kStreams ? c0 + (c1 - c0) * (sidx + 1) / nstreams : c1) - r0);
 
     // The launch's frequency table into shared memory (lane-interleaved layout:
     // the lanes of a warp then read consecutive 16-byte pairs, no bank conflicts).
@@ -128,8 +140,8 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     grid_dep_wait();
 
     const int lane = tid % G;
-    const int group = hchunk * (nt / G) + tid / G;
-    const bool active = group < lay.groups && lane < L;
+    const int group = hchunk * lay.groups_per_cta + (gi - sidx * lay.groups_per_cta);
+    const bool active = gi < nstreams * lay.groups_per_cta && group < lay.groups && lane < L;
     // Groups 0 .. gq-1 take the q heads HPT at a time, the next gq the k heads;
     // the last group of each tensor may hold fewer than HPT heads (nvalid).
     const int gq = (a.n_heads + HPT - 1) / HPT;
@@ -229,7 +241,14 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
             }
             for (int o = G >> 1; o > 0; o >>= 1) {
 #pragma unroll
-                for (int j = 0; j < HPT; ++j) ss[j] += __shfl_xor_sync(0xFFFFFFFFu, ss[j], o);
+                for (int j = 0; j < HPT; ++j) {
+                    if constexpr (kStreams) {  // lanes of other streams may have left the loop
+                        const unsigned gmask = G == 32 ? 0xFFFFFFFFu : ((1u << G) - 1u) << ((tid & 31) & ~(G - 1));
+                        ss[j] += __shfl_xor_sync(gmask, ss[j], o);
+                    } else {
+                        ss[j] += __shfl_xor_sync(0xFFFFFFFFu, ss[j], o);
+                    }
+                }
             }
             if (active) {
                 const int64_t roff = r * a.out_stride;
@@ -259,8 +278,10 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
     // k_out is written +0.0 in the same launch (the input tail is never read).
     const int64_t tail = a.padded_rows - a.rows;
     if (tail > 0 && active) {
-        const int64_t z0 = a.rows + tail * (int64_t)tchunk / token_chunks;
-        const int64_t z1 = a.rows + tail * (int64_t)(tchunk + 1) / token_chunks;
+        const int64_t t0 = a.rows + tail * (int64_t)tchunk / token_chunks;
+        const int64_t t1 = a.rows + tail * (int64_t)(tchunk + 1) / token_chunks;
+        const int64_t z0 = t0 + (t1 - t0) * sidx / nstreams;
+        const int64_t z1 = t0 + (t1 - t0) * (sidx + 1) / nstreams;
         Vec8 zero;
         zero.w[0] = zero.w[1] = zero.w[2] = zero.w[3] = 0u;
         for (int64_t r = z0; r < z1; ++r) {
@@ -298,7 +319,16 @@ bool choose_layout(int n_heads, int head_dim, int heads_per_group, Layout* lay) 
     const int64_t per_cta = kMaxThreads / G;
     const int64_t chunks = (groups + per_cta - 1) / per_cta;
     const int64_t groups_per_cta = (groups + chunks - 1) / chunks;
-    const int64_t threads = (groups_per_cta * G + 31) / 32 * 32;
+    // Few heads (all lane groups of a token in at most half a warp): token
+    // streams side by side fill the warp (3 x 128: 59% -> 80% of the copy
+    // bandwidth).  Measured and left out for wider layouts whose last warp is
+    // only partly idle (12 x 128: 90% -> 85%, 20 x 128: 97% -> 88%).
+    int streams = 1;
+    const int64_t lanes = groups_per_cta * G;
+    if (chunks == 1 && lanes <= 16) streams = (int)(32 / lanes);
+    const int64_t threads = (streams * lanes + 31) / 32 * 32;
+    lay->groups_per_cta = (int)groups_per_cta;
+    lay->streams = streams;
     lay->hpt = hpt;
     lay->lanes = G;
     lay->threads = (int)threads;
@@ -307,14 +337,14 @@ bool choose_layout(int n_heads, int head_dim, int heads_per_group, Layout* lay) 
     return chunks <= 65535;
 }
 
-template <int HPT, bool kMasked>
+template <int HPT, bool kMasked, bool kStreams>
 cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
     const int stage_bytes = HPT * 2 * lay.threads * 16;
     const int table_bytes = (a.head_dim / 2) * 8;
-    const void* fn = reinterpret_cast<const void*>(&qk_rope_kernel<HPT, kMasked>);
+    const void* fn = reinterpret_cast<const void*>(&qk_rope_kernel<HPT, kMasked, kStreams>);
     const int by_regs = blocks_per_sm(fn, lay.threads, table_bytes + 2 * stage_bytes);
     if (by_regs <= 0) return cudaErrorInvalidConfiguration;
     const int stages = pick_stages(by_regs, stage_bytes, table_bytes);
@@ -325,7 +355,8 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
     int64_t want = ((int64_t)per_sm * di.sm_count + lay.head_chunks - 1) / lay.head_chunks;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
     if constexpr (kRowsPerCta > 0) {  // fixed-size chunks instead of one persistent run per CTA
-        const int64_t chunks = (work + kRowsPerCta - 1) / (kRowsPerCta > 0 ? kRowsPerCta : 1);
+        const int64_t per = (kRowsPerCta > 0 ? kRowsPerCta : 1) * lay.streams;  // rows per stream stay kRowsPerCta
+        const int64_t chunks = (work + per - 1) / per;
         if (chunks > want) want = chunks;
     }
     if (want > (1 << 24)) want = 1 << 24;  // the token split covers any count; keeps rows * chunk in range
@@ -342,7 +373,7 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
         last_theta = a.theta;
         last_dim = a.head_dim;
     }
-    return launch_kernel(qk_rope_kernel<HPT, kMasked>, (unsigned)grid, lay.threads, smem, stream, a, lay, (int)want, stages,
+    return launch_kernel(qk_rope_kernel<HPT, kMasked, kStreams>, (unsigned)grid, lay.threads, smem, stream, a, lay, (int)want, stages,
                          table);
 }
 
@@ -356,13 +387,18 @@ bool qk_rope_supported(int n_heads, int head_dim) {
 cudaError_t launch_qk_rmsnorm_rope(const QkRopeArgs& a, cudaStream_t stream) {
     Layout lay;
     if (!choose_layout(a.n_heads, a.head_dim, a.heads_per_group, &lay)) return cudaErrorInvalidValue;
-    const bool masked = a.n_heads % lay.hpt != 0;  // separate instantiation: no predicates otherwise
+    const bool masked = a.n_heads % lay.hpt != 0;  // separate instantiations: no predicates otherwise
+    const bool streams = lay.streams > 1;
+#define TFK_QK_LAUNCH(H) \
+    (masked ? (streams ? launch_h<H, true, true>(a, lay, stream) : launch_h<H, true, false>(a, lay, stream)) \
+            : (streams ? launch_h<H, false, true>(a, lay, stream) : launch_h<H, false, false>(a, lay, stream)))
     switch (lay.hpt) {
-        case 1: return launch_h<1, false>(a, lay, stream);
-        case 2: return masked ? launch_h<2, true>(a, lay, stream) : launch_h<2, false>(a, lay, stream);
-        case 3: return masked ? launch_h<3, true>(a, lay, stream) : launch_h<3, false>(a, lay, stream);
-        default: return masked ? launch_h<4, true>(a, lay, stream) : launch_h<4, false>(a, lay, stream);
+        case 1: return streams ? launch_h<1, false, true>(a, lay, stream) : launch_h<1, false, false>(a, lay, stream);
+        case 2: return TFK_QK_LAUNCH(2);
+        case 3: return TFK_QK_LAUNCH(3);
+        default: return TFK_QK_LAUNCH(4);
     }
+#undef TFK_QK_LAUNCH
 }
 
 }  // namespace tfk

@@ -226,6 +226,11 @@ QK_CASES = [
     (23, 30, 96),      # 2 of 4 heads in the last group, 6 data lanes in a group of 8
     (41, 6, 128),      # 3 heads per lane group
     (19, 9, 64),
+    (33, 12, 128),
+    (18, 20, 128),
+    (7, 3, 128),       # 3 heads per group, two token streams per CTA; fewer rows than streams x 4
+    (25, 2, 128),      # two streams of 16 lanes
+    (9, 4, 64),        # four streams of 8 lanes
     (7, 300, 64),      # many heads: a 2-D grid of token runs x head chunks
     (11, 4, 256),
     (9, 2, 512),
@@ -517,10 +522,11 @@ def test_over_2g_elements_indexing(cuda):
 # fixed-valid mode: the normalisation kernels on the padded buffer directly
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("N,L", [(64, 0), (64, 64), (1000, 777), (4096, 1)])
-def test_fixed_valid_adaln_and_qk(cuda, N, L):
+@pytest.mark.parametrize("N,L,H", [(64, 0, 8), (64, 64, 8), (1000, 777, 8), (4096, 1, 8),
+                                   (1001, 555, 3)])   # 3 heads: two token streams per CTA, tail split too
+def test_fixed_valid_adaln_and_qk(cuda, N, L, H):
     rng = np.random.default_rng(N + 3 * L)
-    hidden, H, D = 1024, 8, 128
+    hidden, D = 1024, 128
     x = rand_bits(rng, (N, hidden))
     q = rand_bits(rng, (N, H * D), 2.0)
     k = rand_bits(rng, (N, H * D))
@@ -583,7 +589,8 @@ def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
                                         (17, 6, 64, 3),
                                         (21, 25, 128, 5),   # 4 heads per lane group, the last one masked,
                                         (9, 30, 96, 3),     # groups spanning two ranks' blocks
-                                        (15, 6, 128, 2), (11, 9, 64, 3)])  # 3 heads per lane group
+                                        (15, 6, 128, 2), (11, 9, 64, 3),   # 3 heads per lane group
+                                        (13, 12, 128, 4), (9, 4, 64, 2)])  # four token streams per CTA
 def test_qk_ulysses_send_layout(cuda, rows, H, D, P):
     rng = np.random.default_rng(rows + 100 * P)
     q = rand_bits(rng, (rows, H * D))
