@@ -83,7 +83,8 @@ __device__ __forceinline__ void load_mod_row(const AdalnArgs& a, int m, const in
 // 3072 x 8192 rows, even at 3072 x 30358; four exact vectors +1.5 points at
 // 4096 and 5120.
 template <int V, int MAXT, bool kExact>
-constexpr int kMinBlocks = V == 1 ? 2 : (V == 2 ? (MAXT <= 256 && kExact ? 3 : 2 * (512 / MAXT)) : 1);
+constexpr int kMinBlocks = V == 1 ? 2 : (V == 2 ? (MAXT <= 256 && kExact ? 3 : 2 * (512 / MAXT))
+                                                : (V == 3 ? 3 : 1));
 
 template <int V, int MAXT, bool kExact>
 __global__ void __launch_bounds__(MAXT, (kMinBlocks<V, MAXT, kExact>))
@@ -246,6 +247,11 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
 // 192-256 threads, i.e. two CTAs of 6-8 warps per SM (measured 74% -> 78% at
 // 6144, +1% at 8192; at 4096 and 5120 four vectors stay ahead).  Beyond
 // 16384 eight vectors do not fit in 128 registers and spill (~40-47%).
+// Hidden a multiple of 768 from 1536 to 6144 takes three whole vectors per
+// thread (64-256 threads, 80 registers): the per-row overhead is spread over
+// 24 elements and the barrier spans fewer warps.  Measured against the
+// shapes above: 5376 68% -> 88%, 6144 78% -> 86%, 4608 83% -> 88%,
+// 1536-2304 +4.5 points, 3072 +1.
 #ifndef TFK_A1_MIN_V
 #define TFK_A1_MIN_V 2
 #endif
@@ -259,6 +265,11 @@ bool choose_shape(int hidden, int* v, int* threads) {
     const int nvec = hidden / 8;
     int first = nvec >= TFK_A1_V4_FROM_NVEC ? 4 : (nvec >= TFK_A1_V2_FROM_NVEC ? TFK_A1_MIN_V : 1);
     if (nvec >= 768 && nvec <= 1024) first = 2;  // hidden 6144-8192: 384-512 threads of 64 registers
+    if (nvec % 96 == 0 && nvec / 3 <= 256 && nvec >= 192) {  // three whole vectors per thread
+        *v = 3;
+        *threads = nvec / 3;
+        return true;
+    }
     for (int cand = first; cand <= 8; cand *= 2) {
         const int t = (nvec + cand - 1) / cand;
         if (t <= (cand == 1 ? kMaxThreadsV1 : kMaxThreads)) {
@@ -312,6 +323,7 @@ cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, cudaStream_t stream) {
             if (threads <= 256)
                 return exact ? launch_v<2, 256, true>(a, threads, stream) : launch_v<2, 256, false>(a, threads, stream);
             return launch_v<2, kMaxThreads, false>(a, threads, stream);
+        case 3: return launch_v<3, 256, true>(a, threads, stream);
         case 4:
             return exact ? launch_v<4, kMaxThreads, true>(a, threads, stream)
                          : launch_v<4, kMaxThreads, false>(a, threads, stream);

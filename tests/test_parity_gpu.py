@@ -130,7 +130,11 @@ ADALN_CASES = [
     (300, 3072, 4, "pairs"),         # two rows alternate per token, then two others
     (129, 5120, 2, "blocks"),
     (1000, 4104, 6, "random"),       # 513 vectors: ragged last thread of a 2-vector layout
-    (200, 6144, 3, "random"),        # 6144-8192: two vectors per thread, 384-512 threads
+    (150, 1536, 3, "pairs"),         # multiples of 768 up to 6144: three vectors per thread
+    (99, 2304, 5, "random"),
+    (60, 5376, 2, "blocks"),
+    (200, 6144, 3, "random"),
+    (120, 7168, 3, "random"),        # 7168-8192: two vectors per thread, 448-512 threads
     (150, 8192, 2, "pairs"),
     (90, 8200, 3, "random"),         # 1025 vectors: back to four per thread, ragged
     (64, 16384, 3, "random"),
