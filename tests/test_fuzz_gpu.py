@@ -1,0 +1,138 @@
+"""Seeded random shapes against the oracle, through the C ABI.
+
+The launchers pick among many kernel instantiations by shape: one, two,
+three, four or eight vectors per thread (whole-vector widths without bounds
+predicates) for RMSNorm+AdaLN; one to four heads per lane group, masked last
+groups and side-by-side token streams for Q/K; one chunk per CTA or several
+whole rows for SwiGLU; 4-row tiles or the column walk for the relayouts.
+Every case here draws its shape from a fixed seed, so a wrong choice or a bad
+edge anywhere in those rules shows up as a parity failure with its shape in
+the test id.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rope_tfk_rmsnorm_gb300 as tfk
+from helpers import Guarded, THREADS, check_close, f32_dev, i32_dev, to_dev
+from test_parity_gpu import gpu_adaln, gpu_qk, gpu_swiglu, mod_params, ora_adaln, ora_qk, ora_swiglu, rand_bits
+
+pytestmark = pytest.mark.gpu
+
+_RNG = np.random.default_rng(20261202)
+
+
+def _hidden(rng):
+    """Widths near the shape thresholds as often as arbitrary multiples of 8."""
+    if rng.random() < 0.5:
+        return int(8 * rng.integers(1, 1025))
+    base = int(rng.choice([512, 768, 1024]))
+    return int(base * rng.integers(1, 9)) + int(rng.choice([0, 0, 8, -8]))
+
+
+def _adaln_cases(n):
+    out = []
+    for _ in range(n):
+        hidden = max(8, _hidden(_RNG))
+        rows = int(_RNG.integers(1, max(2, min(700, 3_000_000 // hidden))))
+        out.append((rows, hidden, int(_RNG.integers(1, 7)), int(_RNG.integers(0, 2 ** 31))))
+    return out
+
+
+def _qk_cases(n):
+    out = []
+    while len(out) < n:
+        D = int(16 * _RNG.integers(1, 17)) if _RNG.random() < 0.85 else 512
+        H = int(_RNG.integers(1, 49))
+        if H * D > 8192:
+            continue
+        rows = int(_RNG.integers(1, 300))
+        out.append((rows, H, D, int(_RNG.integers(0, 2 ** 31))))
+    return out
+
+
+def _swiglu_cases(n):
+    return [(int(_RNG.integers(1, 400)), int(8 * _RNG.integers(1, 1200)), int(_RNG.integers(0, 2 ** 31)))
+            for _ in range(n)]
+
+
+def _ulysses_cases(n):
+    out = []
+    while len(out) < n:
+        P = int(_RNG.integers(1, 9))
+        H = P * int(_RNG.integers(1, 9))
+        D = int(16 * _RNG.integers(1, 17))
+        if H * D > 16384:
+            continue
+        out.append((int(_RNG.integers(1, 200)), H, D, P, int(_RNG.integers(0, 2 ** 31))))
+    return out
+
+
+ADALN = _adaln_cases(40)
+QK = _qk_cases(40)
+SWIGLU = _swiglu_cases(20)
+ULYSSES = _ulysses_cases(16)
+
+
+@pytest.mark.parametrize("rows,hidden,n_mod,seed", ADALN,
+                         ids=[f"{r}x{h}m{m}" for r, h, m, _ in ADALN])
+def test_adaln_random_shapes(cuda, rows, hidden, n_mod, seed):
+    rng = np.random.default_rng(seed)
+    x = rand_bits(rng, (rows, hidden), 2.0)
+    w, sh, sc = mod_params(rng, n_mod, hidden)
+    idx = rng.integers(0, n_mod, rows).astype(np.int32)
+    check_close(gpu_adaln(x, w, sh, sc, idx, 1e-6), ora_adaln(x, w, sh, sc, idx, 1e-6),
+                f"a1 {rows}x{hidden}")
+
+
+@pytest.mark.parametrize("rows,H,D,seed", QK, ids=[f"{r}x{h}x{d}" for r, h, d, _ in QK])
+def test_qk_random_shapes(cuda, rows, H, D, seed):
+    rng = np.random.default_rng(seed)
+    q = rand_bits(rng, (rows, H * D), 2.0)
+    k = rand_bits(rng, (rows, H * D))
+    wq = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    pos = rng.integers(0, 200_000, rows).astype(np.int32)
+    gq, gk = gpu_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6, fused=bool(seed & 1))
+    rq, rk = ora_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6)
+    check_close(gq, rq, f"q {rows}x{H}x{D}")
+    check_close(gk, rk, f"k {rows}x{H}x{D}")
+
+
+@pytest.mark.parametrize("rows,ffn,seed", SWIGLU, ids=[f"{r}x{f}" for r, f, _ in SWIGLU])
+def test_swiglu_random_shapes(cuda, rows, ffn, seed):
+    rng = np.random.default_rng(seed)
+    gu = rand_bits(rng, (rows, 2 * ffn), 3.0)
+    check_close(gpu_swiglu(gu), ora_swiglu(gu), f"swiglu {rows}x{ffn}")
+
+
+@pytest.mark.parametrize("rows,H,D,P,seed", ULYSSES, ids=[f"{r}x{h}x{d}p{p}" for r, h, d, p, _ in ULYSSES])
+def test_ulysses_random_shapes(cuda, rows, H, D, P, seed):
+    """Pack and unpack bit-exact against the oracle's permutation, and the fused
+    Q/K send layout within tolerance."""
+    rng = np.random.default_rng(seed)
+    W = H * D
+    src = rand_bits(rng, (rows, W))
+    packed = tfk.tfk_ulysses_pack(to_dev(src), H, D, P)
+    back = Guarded(rows, W)
+    tfk.tfk_ulysses_unpack(packed, H, D, P, dst=back.view)
+    torch.cuda.synchronize()
+    back.check()
+    want = oracle.ulysses_pack(src, H, D, P)
+    got = packed.contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(want.shape)
+    assert np.array_equal(got, want)
+    assert np.array_equal(back.host(), src)
+
+    q = rand_bits(rng, (rows, W), 2.0)
+    k = rand_bits(rng, (rows, W))
+    wq = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    pos = rng.integers(0, 100_000, rows).astype(np.int32)
+    qs, ks = tfk.tfk_qk_rmsnorm_rope_neox_ulysses(to_dev(q), to_dev(k), f32_dev(wq), f32_dev(wk), i32_dev(pos),
+                                                  H, D, P)
+    torch.cuda.synchronize()
+    rq, rk = ora_qk(q, k, wq, wk, pos, H, D, 10000.0, 1e-6)
+    for got_t, ref, name in ((qs, rq, "q"), (ks, rk, "k")):
+        bits = got_t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        check_close(bits.reshape(-1), oracle.ulysses_pack(ref, H, D, P).reshape(-1), f"ulysses {name}")
