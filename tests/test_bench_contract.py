@@ -58,3 +58,27 @@ def test_prefix_keeps_the_recipe():
 def test_aggregate_is_whole_job_throughput():
     assert bench.aggregate(1000, 1, 2.0) == 500.0
     assert bench.aggregate(1000, 4, 2.0) == 2000.0
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Two ranks launched the way the driver launches N > 1 (gloo on CPU): rank 0
+    prints the one line, the other rank exits 0 without output."""
+    import os
+    import socket
+    import subprocess
+    import sys
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--workload", "tiny", "--steps", "2", "--warmup", "1", "--ref-seconds", "1"]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
