@@ -84,6 +84,8 @@ class Ranks:
             import torch.distributed as dist
             if backend is None:
                 backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":  # bind this rank's GPU before NCCL picks one for barriers
+                torch.cuda.set_device(self.local_rank)
             dist.init_process_group(backend)
             self.pg = True
 
