@@ -335,26 +335,34 @@ class ValidOnly:
 
 
 def time_steps(work, steps: int, warmup: int, ranks: Ranks):
-    """W untimed steps, then exactly `steps` timed steps between barriers and syncs.
-    Returns (total ms on the device, per-kernel mean ms, wall t0, wall t1, per-kernel
-    {p10, p50, p90} ms over the timed steps)."""
+    """W untimed steps, then exactly `steps` timed steps between barriers and syncs,
+    with CUDA events only at the two ends: an event recorded between two launches
+    would make the second wait for the first's full completion and so remove the
+    overlap that programmatic dependent launch gives.  A second pass of the same
+    steps, outside the timed region, records an event between every launch for
+    the per-kernel breakdown.  Returns (total ms of the timed steps on the device,
+    per-kernel mean ms, wall t0, wall t1 of the timed steps, per-kernel {p10, p50,
+    p90} ms)."""
     n_ev = len(work.kernels) + 1
     for _ in range(warmup):
         work.launch()
     torch.cuda.synchronize()
     ranks.barrier()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     start.record()
-    for s in range(steps):
-        work.launch(evs[s])
+    for _ in range(steps):
+        work.launch()
     end.record()
     torch.cuda.synchronize()
     t1 = time.time()
     ranks.barrier()
     total = start.elapsed_time(end)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    for s in range(steps):
+        work.launch(evs[s])
+    torch.cuda.synchronize()
     samples = [[evs[s][j].elapsed_time(evs[s][j + 1]) for s in range(steps)] for j in range(n_ev - 1)]
     per_kernel = [statistics.fmean(v) for v in samples]
     dist = [{f"p{q}": float(np.percentile(v, q)) for q in (10, 50, 90)} for v in samples]
