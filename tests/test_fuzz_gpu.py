@@ -136,3 +136,52 @@ def test_ulysses_random_shapes(cuda, rows, H, D, P, seed):
     for got_t, ref, name in ((qs, rq, "q"), (ks, rk, "k")):
         bits = got_t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
         check_close(bits.reshape(-1), oracle.ulysses_pack(ref, H, D, P).reshape(-1), f"ulysses {name}")
+
+
+def _fixed_valid_cases(n):
+    out = []
+    while len(out) < n:
+        hidden = max(8, _hidden(_RNG))
+        D = int(16 * _RNG.integers(1, 17))
+        H = int(_RNG.integers(1, 33))
+        if H * D > 8192:
+            continue
+        N = int(_RNG.integers(1, max(2, min(400, 2_000_000 // max(hidden, H * D)))))
+        L = int(_RNG.integers(0, N + 1))
+        out.append((N, L, hidden, H, D, int(_RNG.integers(0, 2 ** 31))))
+    return out
+
+
+FIXED = _fixed_valid_cases(16)
+
+
+@pytest.mark.parametrize("N,L,hidden,H,D,seed", FIXED, ids=[f"N{n}L{l}h{hd}q{h}x{d}" for n, l, hd, h, d, _ in FIXED])
+def test_fixed_valid_random_shapes(cuda, N, L, hidden, H, D, seed):
+    """Fixed-valid mode: rows [0, L) computed from the padded buffer, whose NaN
+    tail is never read, and the rest of every output +0.0."""
+    import synth
+    rng = np.random.default_rng(seed)
+    x = rand_bits(rng, (N, hidden))
+    q, k = rand_bits(rng, (N, H * D), 2.0), rand_bits(rng, (N, H * D))
+    for a in (x, q, k):
+        a[L:] = synth.BF16_NAN
+    w, sh, sc = mod_params(rng, 3, hidden)
+    idx = rng.integers(0, 3, max(L, 1)).astype(np.int32)
+    pos = rng.integers(0, 100_000, max(L, 1)).astype(np.int32)
+    wq = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+    y = Guarded(N, hidden)
+    tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(to_dev(x), L, f32_dev(w), f32_dev(sh), f32_dev(sc), i32_dev(idx),
+                                              1e-6, out=y.view)
+    qo, ko = Guarded(N, H * D), Guarded(N, H * D)
+    tfk.tfk_qk_rmsnorm_rope_neox_fixed_valid(to_dev(q), to_dev(k), L, f32_dev(wq), f32_dev(wk), i32_dev(pos),
+                                             H, D, 10000.0, 1e-6, q_out=qo.view, k_out=ko.view)
+    torch.cuda.synchronize()
+    for g in (y, qo, ko):
+        g.check()
+        assert np.all(g.host()[L:] == 0x0000)
+    check_close(y.host(), oracle.rmsnorm_adaln_fixed_valid(x, L, w, sh, sc, idx[:L], 1e-6, threads=THREADS),
+                f"fixed-valid a1 N={N} L={L}")
+    rq, rk = oracle.qk_rmsnorm_rope_neox_fixed_valid(q, k, L, wq, wk, pos[:L], H, D, 10000.0, 1e-6, threads=THREADS)
+    check_close(qo.host(), rq.reshape(N, -1), f"fixed-valid q N={N} L={L}")
+    check_close(ko.host(), rk.reshape(N, -1), f"fixed-valid k N={N} L={L}")
