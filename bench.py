@@ -629,6 +629,31 @@ def run_tfk(args, ranks: Ranks) -> dict | None:
             "valid_only": valid, "cpu_baseline": cpu}
 
 
+class Rotate:
+    """Calls its functions in turn (one per copy of the workload's tensors)."""
+
+    def __init__(self, fns):
+        self.fns, self.i = fns, 0
+
+    def __call__(self):
+        f = self.fns[self.i]
+        self.i = (self.i + 1) % len(self.fns)
+        f()
+
+
+class RotateChain:
+    """The chain step over several copies of a workload's tensors in turn."""
+
+    def __init__(self, chains):
+        self.chains, self.i = chains, 0
+        self.kernels, self.bytes = chains[0].kernels, chains[0].bytes
+
+    def launch(self, ev=None):
+        c = self.chains[self.i]
+        self.i = (self.i + 1) % len(self.chains)
+        c.launch(ev)
+
+
 class Single:
     """One kernel of a workload as a timed unit (the per-kernel sweep)."""
 
@@ -674,11 +699,13 @@ def run_sweep(args, ranks: Ranks):
     torch.cuda.set_device(device)
     peak = measured_peaks()["hbm_gbs"]
     K, W = max(1, min(args.steps, 100)), max(3, args.warmup)
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
     import oracle
     oracle.build()
     for name in [w.strip() for w in args.sweep_workloads.split(",") if w.strip()]:
         wl = synth.get(name) if name == "valid_only" else prefix(synth.get(name), args.rows)
         res = {}
+        buffer_sets = 1
         if name == "valid_only":
             vo = ValidOnly(tfk, wl, device)
             L, N, hd = vo.L, vo.N, wl.hidden
@@ -699,14 +726,21 @@ def run_sweep(args, ranks: Ranks):
                         "qk_rmsnorm_rope_fixed_valid": L}
         else:
             ch = Chain(tfk, wl, device)
-            units = [Single(n, b, f) for n, b, f in zip(
-                ch.kernels, ch.bytes,
-                [lambda: tfk.tfk_rmsnorm_adaln_indexed(ch.d["x"], ch.params["w"], ch.params["shift"],
-                                                       ch.params["scale"], ch.d["idx"], wl.eps, out=ch.out["y"]),
-                 lambda: tfk.tfk_qk_rmsnorm_rope_neox(ch.d["q"], ch.d["k"], ch.params["w_q"], ch.params["w_k"],
-                                                      ch.d["pos"], wl.n_heads, wl.head_dim, wl.theta, wl.eps,
-                                                      q_out=ch.out["q"], k_out=ch.out["k"]),
-                 lambda: tfk.tfk_swiglu(ch.d["gate_up"], out=ch.out["o"])])] + [ch]
+            # Small workloads: rotate over enough copies of every tensor that each
+            # unit's consecutive launches touch more than twice the L2 (HBM-bound
+            # numbers, not L2 hits).
+            copies = min(16, max(1, -(-2 * l2_bytes // min(ch.bytes))))
+            chs = [ch] + [Chain(tfk, wl, device) for _ in range(copies - 1)]
+            makers = [
+                lambda c: lambda: tfk.tfk_rmsnorm_adaln_indexed(c.d["x"], c.params["w"], c.params["shift"],
+                                                                c.params["scale"], c.d["idx"], wl.eps, out=c.out["y"]),
+                lambda c: lambda: tfk.tfk_qk_rmsnorm_rope_neox(c.d["q"], c.d["k"], c.params["w_q"], c.params["w_k"],
+                                                               c.d["pos"], wl.n_heads, wl.head_dim, wl.theta, wl.eps,
+                                                               q_out=c.out["q"], k_out=c.out["k"]),
+                lambda c: lambda: tfk.tfk_swiglu(c.d["gate_up"], out=c.out["o"])]
+            units = [Single(n, b, Rotate([mk(c) for c in chs])) for n, b, mk in zip(ch.kernels, ch.bytes, makers)]
+            units.append(RotateChain(chs))
+            buffer_sets = copies
             rows_for = {}
             if name == "large":  # the Ulysses layouts, 8-way (5 heads per rank)
                 P = 8
@@ -737,8 +771,11 @@ def run_sweep(args, ranks: Ranks):
                     graph_ms=gms, graph_frac=_roof(sum(u.bytes), gms, peak)["frac"], kernels=u.kernels)
         if ranks.rank == 0:
             print(json.dumps({"sweep": name, "workload": workload_config(wl)["workload"], "steps": K,
-                              "peak_gbs": peak, "results": res, "oracle": oracle_rates(wl)}), flush=True)
+                              "peak_gbs": peak, "buffer_sets": buffer_sets, "results": res,
+                              "oracle": oracle_rates(wl)}), flush=True)
         del units
+        if name != "valid_only":
+            ch = chs = None
         torch.cuda.empty_cache()
 
 
