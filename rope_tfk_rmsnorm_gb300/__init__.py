@@ -312,6 +312,5 @@ def tfk_velocity_cache_schedule(num_steps: int, start_ratio: float = 0.2, end_ra
     st = load().tfk_velocity_cache_schedule(num_steps, start_ratio, end_ratio, refresh_interval,
                                             max_consecutive_reuse, ctypes.cast(buf, ctypes.c_void_p),
                                             ctypes.cast(ctypes.pointer(hits), ctypes.c_void_p))
-    if st != TFK_OK:
-        raise TfkError(st, "tfk_velocity_cache_schedule: invalid arguments")
+    _check(st)
     return [bool(buf[i]) for i in range(num_steps)]

@@ -9,7 +9,9 @@
 #include <mutex>
 
 #include "../../include/tfk.h"
+#include "device_scope.h"
 #include "kernels.h"
+#include "status.h"
 
 namespace tfk {
 
@@ -117,11 +119,11 @@ int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes) {
 // ---- status reporting ---------------------------------------------------------
 
 namespace {
-
 thread_local char g_msg[512] = "no error";
 thread_local int g_inject = 0;  // cudaError_t to report instead of the next launch
+}  // namespace
 
-tfk_status fail(tfk_status s, const char* fmt, ...) {
+tfk_status tfk::fail(tfk_status s, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
     vsnprintf(g_msg, sizeof g_msg, fmt, ap);
@@ -129,12 +131,35 @@ tfk_status fail(tfk_status s, const char* fmt, ...) {
     return s;
 }
 
+namespace {
+
+using tfk::fail;
+
 tfk_status ok() { return TFK_OK; }
 
 // Launches go through the library's own (static) CUDA runtime, whose
 // last-error state only this library touches: clear it before a launch so
 // that the check after the launch reports that launch alone.
 void clear_stale_error() { cudaGetLastError(); }
+
+// The CUDA runtime calls on_stream_device() needs (device_scope.h).  The
+// legacy and per-thread default streams belong to the current device.
+struct CudaRuntime {
+    cudaError_t stream_device(cudaStream_t s, int* dev) {
+        if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return cudaGetDevice(dev);
+        return cudaStreamGetDevice(s, dev);
+    }
+    cudaError_t current_device(int* dev) { return cudaGetDevice(dev); }
+    cudaError_t set_device(int dev) { return cudaSetDevice(dev); }
+};
+
+// Runs `launch` with the stream's device current (and the caller's device
+// current again afterwards).
+template <class Fn>
+cudaError_t on_device(void* stream, Fn&& launch) {
+    CudaRuntime rt;
+    return tfk::on_stream_device(rt, static_cast<cudaStream_t>(stream), launch);
+}
 
 tfk_status finish_launch(const char* op, cudaError_t err) {
     if (err != cudaSuccess)
@@ -256,7 +281,8 @@ tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, t
     clear_stale_error();
     tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, padded_rows,
                      hidden, eps};
-    return finish_launch(op, tfk::launch_rmsnorm_adaln(a, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&] { return tfk::launch_rmsnorm_adaln(a, s); }));
 }
 
 // sp_degree == 0: outputs are [padded_rows, out_row_stride] row layouts.
@@ -326,7 +352,8 @@ tfk_status qk_impl(const char* op, const tfk_bf16* q, const tfk_bf16* k, int64_t
     const int64_t gstride = sp_degree > 0 ? rows * hpg * (int64_t)head_dim : 0;
     tfk::QkRopeArgs a{q, k, in_row_stride, q_out, k_out, out_row_stride, q_weight, k_weight,
                       positions, rows, padded_rows, hpg, gstride, n_heads, head_dim, theta, eps};
-    return finish_launch(op, tfk::launch_qk_rmsnorm_rope(a, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&] { return tfk::launch_qk_rmsnorm_rope(a, s); }));
 }
 
 }  // namespace
@@ -404,8 +431,10 @@ static tfk_status relayout_impl(const char* op, const tfk_bf16* src, tfk_bf16* d
     tfk_status st;
     if (take_injected(op, &st)) return st;
     clear_stale_error();
-    return finish_launch(op, tfk::launch_ulysses_relayout(src, dst, row_stride, rows, n_heads, head_dim, sp_degree,
-                                                          pack, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&] {
+        return tfk::launch_ulysses_relayout(src, dst, row_stride, rows, n_heads, head_dim, sp_degree, pack, s);
+    }));
 }
 
 tfk_status tfk_ulysses_pack(const tfk_bf16* src, int64_t src_row_stride, tfk_bf16* dst, int64_t rows,
@@ -440,8 +469,10 @@ tfk_status tfk_swiglu(const tfk_bf16* gate_up, int64_t in_row_stride, tfk_bf16* 
     tfk_status st;
     if (take_injected(op, &st)) return st;
     clear_stale_error();
-    return finish_launch(op, tfk::launch_swiglu(gate_up, in_row_stride, out, out_row_stride, rows, ffn,
-                                                static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&] {
+        return tfk::launch_swiglu(gate_up, in_row_stride, out, out_row_stride, rows, ffn, s);
+    }));
 }
 
 tfk_status tfk_valid_gather(const tfk_bf16* padded, tfk_bf16* compact, int64_t valid_rows,
@@ -460,8 +491,10 @@ tfk_status tfk_valid_gather(const tfk_bf16* padded, tfk_bf16* compact, int64_t v
     tfk_status st;
     if (take_injected(op, &st)) return st;
     clear_stale_error();
-    return finish_launch(op, tfk::launch_valid_gather(padded, compact, valid_rows * hidden / 8,
-                                                      static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&] {
+        return tfk::launch_valid_gather(padded, compact, valid_rows * hidden / 8, s);
+    }));
 }
 
 tfk_status tfk_zero_tail_merge(const tfk_bf16* compact, tfk_bf16* padded, int64_t valid_rows,
@@ -481,9 +514,10 @@ tfk_status tfk_zero_tail_merge(const tfk_bf16* compact, tfk_bf16* padded, int64_
     tfk_status st;
     if (take_injected(op, &st)) return st;
     clear_stale_error();
-    return finish_launch(op, tfk::launch_zero_tail_merge(compact, padded, valid_rows * hidden / 8,
-                                                         padded_rows * hidden / 8,
-                                                         static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&] {
+        return tfk::launch_zero_tail_merge(compact, padded, valid_rows * hidden / 8, padded_rows * hidden / 8, s);
+    }));
 }
 
 }  // extern "C"

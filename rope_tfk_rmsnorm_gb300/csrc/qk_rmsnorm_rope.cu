@@ -185,7 +185,14 @@ __global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const 
         }
     };
 
-    if (nrows > 0) {  // uniform over the CTA
+    // nrows is uniform over one token stream, not over the CTA: with kStreams
+    // the streams of a CTA leave this loop at different iterations.  That is
+    // safe only because the loop holds no CTA-wide barrier and no full-warp
+    // collective: every shuffle below uses the mask of its own G-lane group,
+    // which never spans two streams (a stream owns whole groups).  Adding a
+    // __syncthreads or a full-warp reduction inside this loop would deadlock
+    // whenever kStreams is set.
+    if (nrows > 0) {
         for (int s = 0; s < stages - 1; ++s) {
             if (active && s < nrows) issue(s, s);
             cp_async_commit();

@@ -11,14 +11,26 @@
 #include <cstdio>
 
 #include "../../include/tfk.h"
+#include "status.h"
 
 extern "C" tfk_status tfk_velocity_cache_schedule(int32_t num_steps, double start_ratio, double end_ratio,
                                                   int32_t refresh_interval, int32_t max_consecutive_reuse,
                                                   uint8_t* reuse, int32_t* num_reuse) {
-    if (num_steps < 0 || refresh_interval < 1 || max_consecutive_reuse < 0 || !std::isfinite(start_ratio) ||
-        !std::isfinite(end_ratio) || start_ratio < 0.0 || end_ratio > 1.0 || start_ratio > end_ratio ||
-        (num_steps > 0 && reuse == nullptr))
-        return TFK_ERR_INVALID_ARGUMENT;
+    static const char* op = "tfk_velocity_cache_schedule";
+    using tfk::fail;
+    if (num_steps < 0)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: num_steps = %d < 0", op, num_steps);
+    if (refresh_interval < 1)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: refresh_interval = %d < 1", op, refresh_interval);
+    if (max_consecutive_reuse < 0)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: max_consecutive_reuse = %d < 0", op, max_consecutive_reuse);
+    if (!std::isfinite(start_ratio) || !std::isfinite(end_ratio))
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: start_ratio and end_ratio must be finite", op);
+    if (start_ratio < 0.0 || end_ratio > 1.0 || start_ratio > end_ratio)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: need 0 <= start_ratio (%g) <= end_ratio (%g) <= 1", op,
+                    start_ratio, end_ratio);
+    if (num_steps > 0 && reuse == nullptr)
+        return fail(TFK_ERR_INVALID_ARGUMENT, "%s: reuse is NULL with num_steps = %d", op, num_steps);
     const int32_t limit = max_consecutive_reuse < refresh_interval - 1 ? max_consecutive_reuse : refresh_interval - 1;
     int32_t since_dit = -1;  // reuses since the last DiT call; -1 before the first call
     int32_t hits = 0;

@@ -191,3 +191,21 @@ def test_fixed_valid_validation(lib):
     assert passes_validation(lib, fq)
     assert passes_validation(lib, lambda: fq(qo=A, ko=A + 2 * 1024))
     assert fq(L=20) == INVALID and fq(ko=B + 1024) == INVALID
+
+
+def test_velocity_cache_schedule_sets_the_error_message(lib):
+    buf = (ctypes.c_uint8 * 16)()
+    hits = ctypes.c_int32(0)
+    vp = lambda o: ctypes.cast(o, ctypes.c_void_p)
+    sched = lambda n=10, a=0.2, b=0.8, ri=2, mr=1, r=vp(buf): lib.tfk_velocity_cache_schedule(
+        n, a, b, ri, mr, r, vp(ctypes.pointer(hits)))
+    assert sched() == OK
+    for kwargs, words in [(dict(n=-3), "num_steps = -3"), (dict(ri=0), "refresh_interval = 0"),
+                          (dict(mr=-2), "max_consecutive_reuse = -2"), (dict(a=float("inf")), "finite"),
+                          (dict(a=0.9), "start_ratio (0.9) <= end_ratio (0.8)"), (dict(b=1.5), "<= 1"),
+                          (dict(a=-0.5), "0 <= start_ratio"), (dict(r=None), "reuse is NULL")]:
+        lib.tfk_debug_fail_next_launch(0)
+        assert sched(**kwargs) == INVALID, kwargs
+        m = msg(lib)
+        assert m.startswith("tfk_velocity_cache_schedule: ") and words in m, (kwargs, m)
+    assert sched(n=0, r=None) == OK                                         # no steps: reuse may be NULL

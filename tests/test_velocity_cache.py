@@ -52,7 +52,7 @@ def test_oracle_schedule_properties():
     assert sum(s3) > sum(s)
 
 
-def test_library_schedule_matches_the_oracle(lib):
+def _library_matches_oracle():
     g = golden()
     assert sum(tfk.tfk_velocity_cache_schedule(49)) == g["cache_hits"]
     for n, (a, b), ri, mr in itertools.product([0, 1, 2, 5, 10, 48, 49, 50, 100, 257],
@@ -62,8 +62,23 @@ def test_library_schedule_matches_the_oracle(lib):
             (n, a, b, ri, mr)
 
 
+def test_library_schedule_matches_the_oracle(lib):
+    _library_matches_oracle()
+
+
+@pytest.mark.gpu
+def test_library_schedule_matches_the_oracle_on_the_gpu_host(lib):
+    """The same check in the GPU run, where the library is built on the GPU host itself."""
+    _library_matches_oracle()
+
+
 def test_library_schedule_rejects_bad_arguments(lib):
-    for args in [(-1, 0.2, 0.8, 2, 1), (10, 0.8, 0.2, 2, 1), (10, -0.1, 0.8, 2, 1), (10, 0.2, 1.5, 2, 1),
-                 (10, 0.2, 0.8, 0, 1), (10, 0.2, 0.8, 2, -1), (10, float("nan"), 0.8, 2, 1)]:
-        with pytest.raises(tfk.TfkError):
+    for args, words in [((-1, 0.2, 0.8, 2, 1), "num_steps = -1"), ((10, 0.8, 0.2, 2, 1), "<= end_ratio"),
+                        ((10, -0.1, 0.8, 2, 1), "0 <= start_ratio"), ((10, 0.2, 1.5, 2, 1), "<= 1"),
+                        ((10, 0.2, 0.8, 0, 1), "refresh_interval = 0"),
+                        ((10, 0.2, 0.8, 2, -1), "max_consecutive_reuse = -1"),
+                        ((10, float("nan"), 0.8, 2, 1), "finite")]:
+        with pytest.raises(tfk.TfkError) as e:
             tfk.tfk_velocity_cache_schedule(*args)
+        assert e.value.status == 1 and "tfk_velocity_cache_schedule" in str(e.value) and words in str(e.value), \
+            (args, str(e.value))
