@@ -39,6 +39,12 @@ MUTATIONS = [
     ("merge_negative_zero_tail", ": (uint16_t)0x0000;", ": (uint16_t)0x8000;"),
     ("gather_off_by_one", "for (int64_t i = 0; i < valid_rows; ++i)\n        for (int32_t j = 0; j < hidden; ++j)\n            compact",
      "for (int64_t i = 0; i + 1 < valid_rows; ++i)\n        for (int32_t j = 0; j < hidden; ++j)\n            compact"),
+    ("rope_one_middle_frequency", "double angle = (double)pos[t] * inv_freq;",
+     "double angle = (double)pos[t] * (i == 37 ? inv_freq * 1.001 : inv_freq);"),
+    ("rope_last_pair_unrotated", "double c = cos(angle), s = sin(angle);",
+     "double c = i == half - 1 ? 1.0 : cos(angle), s = i == half - 1 ? 0.0 : sin(angle);"),
+    ("adaln_last_column_unmodulated", "y[t * hidden + j] = n * (1.0 + s) + b;",
+     "y[t * hidden + j] = j == hidden - 1 ? n : n * (1.0 + s) + b;"),
     ("round_half_up", "double n = rint(a / quantum);", "double n = floor(a / quantum + 0.5);"),
     ("round_truncates", "double n = rint(a / quantum);", "double n = floor(a / quantum);"),
 ]

@@ -8,6 +8,7 @@ transposed operand, a mean taken over the wrong axis) fails at least one.
 No GPU is involved.
 """
 import math
+import struct
 
 import numpy as np
 import pytest
@@ -424,3 +425,151 @@ def test_fixed_valid_oracle_is_the_plain_definition_then_zeros():
     qf, kf = oracle.qk_rmsnorm_rope_neox(q, q, wq, wq, pos, 2, 64, 10000.0, 1e-6)
     qp, kp = oracle.qk_rmsnorm_rope_neox_fixed_valid(q, q, 30, wq, wq, pos, 2, 64, 10000.0, 1e-6)
     assert np.array_equal(qp[:30], qf[:30]) and np.all(qp[30:] == 0.0) and np.array_equal(kp[:30], kf[:30])
+
+
+# ---------------------------------------------------------------------------
+# brute force on 4 tokens: every operation restated as scalar long-double
+# loops written here (no code of oracle.c), RoPE as an explicit D x D
+# block-rotation matrix per token, compared with the oracle's loop form
+# ---------------------------------------------------------------------------
+
+LD = np.longdouble
+BRUTE_POS = np.array([0, 1, 4096, 75599], np.int32)   # first, second, a mid and the largest workload position
+
+
+def _bf16_value(bits: int) -> float:
+    """Value of one raw bf16 pattern: the top half of an IEEE binary32 (struct, not the oracle)."""
+    return struct.unpack("<f", struct.pack("<I", int(bits) << 16))[0]
+
+
+def _row_ld(bits_row) -> list:
+    return [LD(_bf16_value(b)) for b in bits_row]
+
+
+def _brute_adaln(x_bits, w, shift, scale, idx, eps):
+    rows, hidden = x_bits.shape
+    out = np.empty((rows, hidden), LD)
+    for t in range(rows):
+        xs = _row_ld(x_bits[t])
+        ss = LD(0)
+        for v in xs:
+            ss += v * v
+        r = LD(1) / np.sqrt(ss / LD(hidden) + LD(eps))
+        m = int(idx[t])
+        for j in range(hidden):
+            out[t, j] = xs[j] * r * LD(float(w[j])) * (LD(1) + LD(float(scale[m, j]))) + LD(float(shift[m, j]))
+    return out
+
+
+def _rotation_matrix(pos: int, D: int, base: float) -> np.ndarray:
+    """The NeoX rotary map of one token as a D x D matrix: plane (i, i + D/2) turned by
+    pos * base^(-2i/D), every other coordinate untouched by that plane's rotation."""
+    half = D // 2
+    R = np.zeros((D, D), LD)
+    for i in range(half):
+        ang = LD(int(pos)) * np.power(LD(base), LD(-2 * i) / LD(D))
+        c, s_ = np.cos(ang), np.sin(ang)
+        R[i, i], R[i, i + half] = c, -s_
+        R[i + half, i], R[i + half, i + half] = s_, c
+    return R
+
+
+def _brute_head_norm(bits_row, H, D, w, eps) -> np.ndarray:
+    out = np.empty((H, D), LD)
+    for h in range(H):
+        v = _row_ld(bits_row[h * D:(h + 1) * D])
+        ss = LD(0)
+        for a in v:
+            ss += a * a
+        r = LD(1) / np.sqrt(ss / LD(D) + LD(eps))
+        for d in range(D):
+            out[h, d] = v[d] * r * LD(float(w[d]))
+    return out
+
+
+def _rope_tol(pos, n) -> np.ndarray:
+    """1e-12, plus what fp64 can do no better than: the oracle forms pos * base^(-2i/D) in
+    double (pow within 1 ulp, the product within half an ulp), so its angle is off by at
+    most ~3.3e-16 * |pos| rad, which moves a pair of norm <= sqrt(2) max|n| by that much."""
+    return 1e-12 + 5e-16 * np.abs(pos.astype(np.float64))[:, None, None] * np.abs(n).max(axis=(1, 2))[:, None, None]
+
+
+@pytest.mark.parametrize("D", [8, 64, 128])
+def test_brute_force_4_tokens_qk_rotation_matrix(D):
+    H, eps, base = 2, 1e-6, 10000.0
+    rng = np.random.default_rng(D)
+    q = bf16(rng.standard_normal((4, H * D)) * 2.0)
+    k = bf16(rng.standard_normal((4, H * D)) * 0.5)
+    wq = (1 + 0.2 * rng.standard_normal(D)).astype(np.float32)
+    wk = (1 + 0.2 * rng.standard_normal(D)).astype(np.float32)
+    qo, ko = oracle.qk_rmsnorm_rope_neox(q, k, wq, wk, BRUTE_POS, H, D, base, eps)
+    for bits, w, got in ((q, wq, qo), (k, wk, ko)):
+        n = np.stack([_brute_head_norm(bits[t], H, D, w, eps) for t in range(4)])     # [4, H, D]
+        expect = np.stack([(_rotation_matrix(BRUTE_POS[t], D, base) @ n[t].T).T for t in range(4)])
+        err = np.abs(got - expect.astype(np.float64))
+        tol = _rope_tol(BRUTE_POS, n.astype(np.float64))
+        assert np.all(err <= tol), f"D={D}: worst {err.max()!r} at {np.unravel_index(np.argmax(err - tol), err.shape)}"
+    # the separate halves of the oracle agree with the same matrices
+    rot = oracle.rope_neox(oracle.head_rmsnorm(q, H, D, wq, eps), BRUTE_POS, base)
+    assert np.array_equal(rot, qo)
+
+
+def test_brute_force_4_tokens_adaln():
+    rng = np.random.default_rng(44)
+    for hidden, n_mod in ((8, 1), (64, 3), (520, 4)):
+        x = bf16(rng.standard_normal((4, hidden)) * np.array([[0.01], [1.0], [7.0], [50.0]]))
+        w = (1 + 0.1 * rng.standard_normal(hidden)).astype(np.float32)
+        shift = (0.2 * rng.standard_normal((n_mod, hidden))).astype(np.float32)
+        scale = (0.2 * rng.standard_normal((n_mod, hidden))).astype(np.float32)
+        idx = (np.arange(4) % n_mod).astype(np.int32)[::-1].copy()
+        got = oracle.rmsnorm_adaln_indexed(x, w, shift, scale, idx, 1e-6)
+        expect = _brute_adaln(x, w, shift, scale, idx, 1e-6).astype(np.float64)
+        assert np.abs(got - expect).max() <= 1e-12, (hidden, np.abs(got - expect).max())
+
+
+def test_brute_force_4_tokens_swiglu():
+    rng = np.random.default_rng(45)
+    ffn = 40
+    gu = bf16(rng.standard_normal((4, 2 * ffn)) * 4.0)
+    got = oracle.swiglu(gu)
+    for t in range(4):
+        row = _row_ld(gu[t])
+        for j in range(ffn):
+            g, u = row[j], row[ffn + j]
+            expect = g / (LD(1) + np.exp(-g)) * u
+            assert abs(got[t, j] - float(expect)) <= 1e-12, (t, j)
+
+
+def test_brute_force_4_tokens_gather_merge_and_fixed_valid():
+    rng = np.random.default_rng(46)
+    hidden = 24
+    padded = rng.integers(0, 65536, (4, hidden), dtype=np.uint32).astype(np.uint16)
+    x = bf16(rng.standard_normal((4, hidden)))
+    w = np.ones(hidden, np.float32)
+    zeros = np.zeros((1, hidden), np.float32)
+    for L in range(5):
+        rows = [[int(b) for b in padded[i]] for i in range(4)]
+        compact = [rows[i][:] for i in range(L)]
+        merged = [compact[i][:] if i < L else [0] * hidden for i in range(4)]
+        assert oracle.valid_gather(padded, L).tolist() == compact
+        assert oracle.zero_tail_merge(oracle.valid_gather(padded, L), 4).tolist() == merged
+        fv = oracle.rmsnorm_adaln_fixed_valid(x, L, w, zeros, zeros, np.zeros(L, np.int32), 1e-6)
+        for i in range(4):
+            if i < L:
+                assert np.abs(fv[i] - _brute_adaln(x[i:i + 1], w, zeros, zeros, [0], 1e-6)[0].astype(np.float64)).max() <= 1e-12
+            else:
+                assert np.all(fv[i] == 0.0) and not np.any(np.signbit(fv[i]))
+
+
+def test_brute_force_4_tokens_ulysses_pack():
+    rng = np.random.default_rng(47)
+    H, D = 6, 8
+    x = rng.integers(0, 65536, (4, H * D), dtype=np.uint32).astype(np.uint16)
+    for P in (1, 2, 3, 6):
+        got = oracle.ulysses_pack(x, H, D, P)
+        hp = H // P
+        for p in range(P):
+            for t in range(4):
+                for j in range(hp):
+                    for d in range(D):
+                        assert got[p, t, j, d] == x[t, (p * hp + j) * D + d]
