@@ -105,12 +105,18 @@ def bf16_to_f64(b: np.ndarray) -> np.ndarray:
         return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def round_bf16(v: np.ndarray) -> np.ndarray:
-    """fp64 -> bf16 bits, nearest with ties to even (one rounding)."""
+def round_bf16(v: np.ndarray, threads: int = 1) -> np.ndarray:
+    """fp64 -> bf16 bits, nearest with ties to even (one rounding); `threads` splits the
+    elements over host threads (the result does not depend on the split)."""
     v = np.ascontiguousarray(v, dtype=np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
     if v.size:
-        _load().oracle_round_bf16(_p(v), v.size, _p(out))
+        lib = _load()
+
+        def part(s, e):
+            if e > s:
+                lib.oracle_round_bf16(_p(v, s), e - s, _p(out, s))
+        _run(part, v.size, threads)
     return out
 
 

@@ -143,10 +143,28 @@ tfk_status ok() { return TFK_OK; }
 void clear_stale_error() { cudaGetLastError(); }
 
 // The CUDA runtime calls on_stream_device() needs (device_scope.h).  The
-// legacy and per-thread default streams belong to the current device.
+// stream's device is the current one, without asking the stream, when:
+// - the process sees a single device;
+// - the stream is a legacy or per-thread default stream;
+// - the stream is being captured into a graph: the query is refused during a
+//   global-mode capture (error 900, and the capture is invalidated), and a
+//   capture is made with its stream's device current, as torch.cuda.graph does.
 struct CudaRuntime {
     cudaError_t stream_device(cudaStream_t s, int* dev) {
-        if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return cudaGetDevice(dev);
+        static const int n_devices = [] {
+            int n = 0;
+            if (cudaGetDeviceCount(&n) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            return n;
+        }();
+        if (n_devices == 1 || s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread)
+            return cudaGetDevice(dev);
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        const cudaError_t e = cudaStreamIsCapturing(s, &cap);
+        if (e != cudaSuccess) return e;
+        if (cap != cudaStreamCaptureStatusNone) return cudaGetDevice(dev);
         return cudaStreamGetDevice(s, dev);
     }
     cudaError_t current_device(int* dev) { return cudaGetDevice(dev); }

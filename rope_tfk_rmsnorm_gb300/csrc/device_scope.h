@@ -10,7 +10,8 @@
 // attributes and occupancy are then looked up for that device too) and makes
 // the caller's device current again afterwards, whether the launch succeeded
 // or not.  The legacy and per-thread default streams belong to the current
-// device.
+// device; so does a stream under graph capture, which may not be queried
+// (the runtime adapter in api.cu takes these cases without asking the stream).
 //
 // Header-only and templated over the runtime calls so that the host logic can
 // be tested on a machine without a GPU against a fake runtime.

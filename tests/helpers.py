@@ -66,7 +66,7 @@ def check_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rto
     err = np.abs(g - ref)
     bound = atol + rtol * np.abs(ref)
     bad = err > bound
-    rounded = oracle.round_bf16(ref)
+    rounded = oracle.round_bf16(ref, threads=THREADS)
     stats = {
         "n": int(ref.size),
         "max_abs": float(err.max()) if err.size else 0.0,
@@ -78,3 +78,20 @@ def check_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rto
         raise AssertionError(f"{what}: {int(bad.sum())} of {err.size} elements out of tolerance; worst at "
                              f"{i}: gpu {g[i]!r} oracle {ref[i]!r}; {stats}")
     return stats
+
+
+class Stats:
+    """Running totals of check_close results over the row blocks of one output."""
+
+    def __init__(self, what: str):
+        self.what, self.n, self.max_abs, self.max_rel, self.equal = what, 0, 0.0, 0.0, 0.0
+
+    def add(self, s: dict):
+        self.n += s["n"]
+        self.max_abs = max(self.max_abs, s["max_abs"])
+        self.max_rel = max(self.max_rel, s["max_rel"])
+        self.equal += s["bit_equal"] * s["n"]
+
+    def summary(self) -> dict:
+        return {"what": self.what, "n": self.n, "max_abs": self.max_abs, "max_rel": self.max_rel,
+                "bit_equal": self.equal / max(1, self.n)}

@@ -59,6 +59,11 @@ def test_round_matches_torch_rne_cast_of_fp32_values():
     assert np.array_equal(oracle.round_bf16(x.astype(np.float64)), bf16(x))
 
 
+def test_round_thread_split_changes_nothing():
+    v = RNG.standard_normal(100003) * 10.0 ** RNG.integers(-8, 8, 100003)
+    assert np.array_equal(oracle.round_bf16(v, threads=7), oracle.round_bf16(v))
+
+
 def test_round_ties_go_to_even_and_off_ties_go_to_nearest():
     lo = bf16(RNG.uniform(-100, 100, 5000))
     lo = lo[(lo & 0x7F80) != 0x7F80]

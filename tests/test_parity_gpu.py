@@ -5,9 +5,10 @@ Bit-exact for gather/merge; |gpu - oracle| <= 2e-2 + 1e-2*|oracle| per
 element for the floating-point kernels.  Every output buffer is surrounded by
 canary rows (and canary padding columns where the stride is wider than the
 row), which must come back untouched.  Small and ragged cases are compared in
-full; the full-size workloads run at full size on the GPU and are compared on
-a seeded sample of rows that the oracle recomputes from freshly generated
-inputs.
+full, and so are the full-size workloads (75,600 and 56,320 tokens, the
+32,768-row valid-only buffer and the 8-rank Ulysses send layout), in blocks
+of rows that bound host memory; a few extra shapes beyond the workloads are
+compared on seeded samples of rows.
 """
 import numpy as np
 import pytest
@@ -16,7 +17,7 @@ import torch
 import oracle
 import rope_tfk_rmsnorm_gb300 as tfk
 import synth
-from helpers import Guarded, THREADS, check_close, f32_dev, i32_dev, to_dev, to_host
+from helpers import Guarded, Stats, THREADS, check_close, f32_dev, i32_dev, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -425,42 +426,64 @@ def test_valid_only_pipeline(cuda):
         assert np.all(merged[L:] == 0x0000) and not np.any(np.isnan(oracle.bf16_to_f64(merged)))
 
 
-def _sampled_chain(wl, n_sample=192):
-    """Full-size chain on the GPU; the oracle recomputes a seeded sample of rows."""
-    rows = synth.sample_rows(wl, n_sample)
+BLOCK = 4096  # rows per oracle block: bounds host memory on the full-size workloads
+
+
+def _blocks(n: int, block: int = BLOCK):
+    return [(s, min(n, s + block)) for s in range(0, n, block)]
+
+
+def _host_and_dev(wl, tag: str, rows: int):
+    """The first `rows` rows of an activation input, on the host and on the device."""
+    host = synth.activation(wl, tag, rows=np.arange(rows))
+    return host, to_dev(host)
+
+
+def _report(stats: dict):
+    for st in stats.values():
+        print(st)
+
+
+def _full_chain(wl):
+    """Full-size chain on the GPU, every element of a1, a2 and a3 compared with the oracle,
+    in blocks of rows (the oracle on all host threads)."""
     p, pd = _params_dev(wl)
-    idx_all, pos_all = synth.mod_index(wl), synth.positions(wl)
-    stats = {}
-    # one step at a time to bound device memory: inputs of a step are freed before the next
-    _, dev = _inputs_dev(wl, ["x"])
-    y = tfk.tfk_rmsnorm_adaln_indexed(dev["x"], pd["w"], pd["shift"], pd["scale"], i32_dev(idx_all), wl.eps)
+    idx, pos = synth.mod_index(wl), synth.positions(wl)
+    T = wl.rows
+    stats = {k: Stats(f"{wl.name} {k}") for k in ("a1", "a2q", "a2k", "a3")}
+    # one step at a time to bound host and device memory
+    x, xd = _host_and_dev(wl, "x", T)
+    y = tfk.tfk_rmsnorm_adaln_indexed(xd, pd["w"], pd["shift"], pd["scale"], i32_dev(idx), wl.eps)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(y.float()).all())
-    ys = to_host(y[torch.from_numpy(rows).cuda()])
-    del dev, y
-    xs = synth.activation(wl, "x", rows=rows)
-    stats["a1"] = check_close(ys, ora_adaln(xs, p["w"], p["shift"], p["scale"], idx_all[rows], wl.eps),
-                              f"{wl.name} a1")
-    _, dev = _inputs_dev(wl, ["q", "k"])
-    qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(dev["q"], dev["k"], pd["w_q"], pd["w_k"], i32_dev(pos_all),
-                                          wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+    del xd
+    for s, e in _blocks(T):
+        stats["a1"].add(check_close(to_host(y[s:e]), ora_adaln(x[s:e], p["w"], p["shift"], p["scale"], idx[s:e],
+                                                                wl.eps), f"{wl.name} a1 rows {s}:{e}"))
+    del x, y
+    q, qd = _host_and_dev(wl, "q", T)
+    k, kd = _host_and_dev(wl, "k", T)
+    qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(qd, kd, pd["w_q"], pd["w_k"], i32_dev(pos), wl.n_heads, wl.head_dim,
+                                          wl.theta, wl.eps)
     torch.cuda.synchronize()
-    sel = torch.from_numpy(rows).cuda()
-    qs, ks = to_host(qo[sel]), to_host(ko[sel])
-    del dev, qo, ko
-    rq, rk = ora_qk(synth.activation(wl, "q", rows=rows), synth.activation(wl, "k", rows=rows),
-                    p["w_q"], p["w_k"], pos_all[rows], wl.n_heads, wl.head_dim, wl.theta, wl.eps)
-    stats["a2q"] = check_close(qs, rq, f"{wl.name} a2 q")
-    stats["a2k"] = check_close(ks, rk, f"{wl.name} a2 k")
-    _, dev = _inputs_dev(wl, ["gate_up"])
-    o = tfk.tfk_swiglu(dev["gate_up"])
+    del qd, kd
+    for s, e in _blocks(T):
+        rq, rk = ora_qk(q[s:e], k[s:e], p["w_q"], p["w_k"], pos[s:e], wl.n_heads, wl.head_dim, wl.theta, wl.eps)
+        stats["a2q"].add(check_close(to_host(qo[s:e]), rq, f"{wl.name} a2 q rows {s}:{e}"))
+        stats["a2k"].add(check_close(to_host(ko[s:e]), rk, f"{wl.name} a2 k rows {s}:{e}"))
+    del q, k, qo, ko
+    gu, gud = _host_and_dev(wl, "gate_up", T)
+    o = tfk.tfk_swiglu(gud)
     torch.cuda.synchronize()
-    assert bool(torch.isfinite(o.float()).all())
-    os_ = to_host(o[torch.from_numpy(rows).cuda()])
-    del dev, o
-    stats["a3"] = check_close(os_, ora_swiglu(synth.activation(wl, "gate_up", rows=rows)), f"{wl.name} a3")
+    del gud
+    for s, e in _blocks(T):
+        stats["a3"].add(check_close(to_host(o[s:e]), ora_swiglu(gu[s:e]), f"{wl.name} a3 rows {s}:{e}"))
+    del gu, o
     torch.cuda.empty_cache()
-    return stats
+    out = {k: v.summary() for k, v in stats.items()}
+    _report(out)
+    assert out["a1"]["n"] == T * wl.hidden and out["a3"]["n"] == T * wl.ffn
+    assert out["a2q"]["n"] == out["a2k"]["n"] == T * wl.n_heads * wl.head_dim
+    return out
 
 
 @pytest.mark.parametrize("rows,hidden", [(120000, 512), (50000, 3072), (20000, 16384)])
@@ -487,12 +510,14 @@ def test_adaln_chunked_schedule_sampled(cuda, rows, hidden):
     check_close(got, ora_adaln(xs, w, sh, sc, idx[sample], 1e-6), f"a1 chunked hidden {hidden}")
 
 
-def test_large_sampled(cuda):
-    _sampled_chain(synth.get("large"))
+def test_large_full(cuda):
+    """The 75,600-token workload: every output element of the chain (including all 756
+    outlier rows) against the oracle."""
+    _full_chain(synth.get("large"))
 
 
-def test_per_frame_sampled(cuda):
-    _sampled_chain(synth.get("per_frame"))
+def test_per_frame_full(cuda):
+    _full_chain(synth.get("per_frame"))
 
 
 def test_over_2g_elements_indexing(cuda):
@@ -560,7 +585,8 @@ def test_fixed_valid_adaln_and_qk(cuda, N, L, H):
 
 
 def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
-    """The valid-only workload without gather and merge: in place on the padded buffers."""
+    """The valid-only workload without gather and merge: in place on the padded buffers,
+    every valid element against the oracle and every tail element +0.0."""
     wl = synth.get("valid_only")
     N, L = wl.rows, synth.valid_len(wl)
     host, dev = _inputs_dev(wl, ["x", "q", "k"])
@@ -574,15 +600,20 @@ def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
                                              q_out=dev["q"], k_out=dev["k"])
     torch.cuda.synchronize()
     y, qo, ko = (to_host(dev[t]) for t in ("x", "q", "k"))
+    del dev
     for a in (y, qo, ko):
         assert np.all(a[L:] == 0x0000)
-    sample = synth.sample_rows(wl, 256, limit=L)
-    check_close(y[sample], ora_adaln(host["x"][sample], p["w"], p["shift"], p["scale"], idx[sample], wl.eps),
-                "valid-only fixed-valid a1")
-    rq, rk = ora_qk(host["q"][sample], host["k"][sample], p["w_q"], p["w_k"], pos[sample], wl.n_heads,
-                    wl.head_dim, wl.theta, wl.eps)
-    check_close(qo[sample], rq, "valid-only fixed-valid q")
-    check_close(ko[sample], rk, "valid-only fixed-valid k")
+    stats = {k: Stats(f"valid_only fixed-valid {k}") for k in ("a1", "a2q", "a2k")}
+    for s, e in _blocks(L):
+        stats["a1"].add(check_close(y[s:e], ora_adaln(host["x"][s:e], p["w"], p["shift"], p["scale"], idx[s:e],
+                                                       wl.eps), f"valid-only fixed-valid a1 rows {s}:{e}"))
+        rq, rk = ora_qk(host["q"][s:e], host["k"][s:e], p["w_q"], p["w_k"], pos[s:e], wl.n_heads,
+                        wl.head_dim, wl.theta, wl.eps)
+        stats["a2q"].add(check_close(qo[s:e], rq, f"valid-only fixed-valid q rows {s}:{e}"))
+        stats["a2k"].add(check_close(ko[s:e], rk, f"valid-only fixed-valid k rows {s}:{e}"))
+    out = {k: v.summary() for k, v in stats.items()}
+    _report(out)
+    assert out["a1"]["n"] == L * wl.hidden
 
 
 # ---------------------------------------------------------------------------
@@ -631,11 +662,36 @@ def test_ulysses_pack_unpack_bit_exact(cuda, rows, H, D, P, stride_pad):
     assert np.array_equal(back.host(), x)
 
 
-@pytest.mark.parametrize("P", [4, 8])
-def test_qk_ulysses_full_size_sampled(cuda, P):
-    """The fused Ulysses packing on the 75,600-token workload (40 heads: 10 or 5 heads per
-    rank), sampled rows against the oracle."""
+def test_qk_ulysses_full_size(cuda):
+    """The fused Ulysses packing on the 75,600-token workload for 8 ranks (5 heads per rank):
+    every element of both send buffers against the oracle's permutation of its Q/K result."""
     wl = synth.get("large")
+    P, T, H, D = 8, wl.rows, wl.n_heads, wl.head_dim
+    p, pd = _params_dev(wl)
+    pos = synth.positions(wl)
+    q, qd = _host_and_dev(wl, "q", T)
+    k, kd = _host_and_dev(wl, "k", T)
+    qs, ks = tfk.tfk_qk_rmsnorm_rope_neox_ulysses(qd, kd, pd["w_q"], pd["w_k"], i32_dev(pos), H, D, P)
+    torch.cuda.synchronize()
+    del qd, kd
+    stats = {"q": Stats("ulysses q P=8"), "k": Stats("ulysses k P=8")}
+    for s, e in _blocks(T):
+        rq, rk = ora_qk(q[s:e], k[s:e], p["w_q"], p["w_k"], pos[s:e], H, D, wl.theta, wl.eps)
+        stats["q"].add(check_close(to_host(qs[:, s:e]).reshape(-1), oracle.ulysses_pack(rq, H, D, P).reshape(-1),
+                                   f"ulysses q P={P} rows {s}:{e}"))
+        stats["k"].add(check_close(to_host(ks[:, s:e]).reshape(-1), oracle.ulysses_pack(rk, H, D, P).reshape(-1),
+                                   f"ulysses k P={P} rows {s}:{e}"))
+    out = {k: v.summary() for k, v in stats.items()}
+    _report(out)
+    assert out["q"]["n"] == out["k"]["n"] == T * H * D
+    del qs, ks
+    torch.cuda.empty_cache()
+
+
+def test_qk_ulysses_full_size_sampled_p4(cuda):
+    """The same on 4 ranks (10 heads per rank), on a seeded sample of rows."""
+    wl = synth.get("large")
+    P = 4
     p, pd = _params_dev(wl)
     rows = synth.sample_rows(wl, 96)
     _, dev = _inputs_dev(wl, ["q", "k"])

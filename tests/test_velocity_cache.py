@@ -1,5 +1,7 @@
 """Conservative DiT velocity-cache schedule: the oracle against the page's own
-counts, and the library's host implementation against the oracle (no GPU)."""
+counts, the library's host implementation against the oracle (no GPU), and
+the schedule driving the chained GPU path over a 49-step run: a hit launches
+nothing and hands back the previous step's velocity."""
 import itertools
 import os
 
@@ -82,3 +84,76 @@ def test_library_schedule_rejects_bad_arguments(lib):
             tfk.tfk_velocity_cache_schedule(*args)
         assert e.value.status == 1 and "tfk_velocity_cache_schedule" in str(e.value) and words in str(e.value), \
             (args, str(e.value))
+
+
+@pytest.mark.gpu
+def test_schedule_gates_the_chain_on_the_gpu(lib, cuda):
+    """49 denoising steps of the 320-token chain (RMSNorm+AdaLN, Q/K RMSNorm+RoPE, SwiGLU
+    standing in for the DiT call), gated by the library's schedule with the page's defaults
+    (TeleFuser PR #38, section 3 and the section 1 table: 34 DiT calls, 15 hits).  A DiT step
+    runs the chain on that step's inputs and its outputs become the cached velocity; a hit
+    launches nothing and returns the cached buffers.  Checked: 34 chain runs and 3 * 34
+    kernel launches of this library (counted by the CUDA profiler), every hit bit-identical
+    to the step before it, every computed step within tolerance of the oracle."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+
+    import oracle
+    import synth
+    from helpers import THREADS, check_close, f32_dev, i32_dev, to_dev, to_host
+
+    g = golden()
+    sched = tfk.tfk_velocity_cache_schedule(g["steps"])
+    base = synth.get("tiny")
+    p = synth.params(base)
+    pd = {k: f32_dev(v) for k, v in p.items()}
+    idx, pos = synth.mod_index(base), synth.positions(base)
+    idx_d, pos_d = i32_dev(idx), i32_dev(pos)
+    inputs = []
+    for i in range(g["steps"]):  # the step's DiT inputs: a fresh draw per step
+        wl = dataclasses.replace(base, seed=1000 + i)
+        inputs.append({t: synth.activation(wl, t) for t in ("x", "q", "k", "gate_up")})
+    dev_inputs = [{t: to_dev(a) for t, a in step.items()} for step in inputs]
+    torch.cuda.synchronize()
+
+    velocity, calls, handed = None, [], []
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for i, hit in enumerate(sched):
+            if hit:
+                assert velocity is not None, "a hit before any DiT call"
+                out = velocity
+            else:
+                d = dev_inputs[i]
+                y = tfk.tfk_rmsnorm_adaln_indexed(d["x"], pd["w"], pd["shift"], pd["scale"], idx_d, base.eps)
+                qo, ko = tfk.tfk_qk_rmsnorm_rope_neox(d["q"], d["k"], pd["w_q"], pd["w_k"], pos_d, base.n_heads,
+                                                      base.head_dim, base.theta, base.eps)
+                o = tfk.tfk_swiglu(d["gate_up"])
+                out = velocity = (y, qo, ko, o)
+                calls.append(i)
+            handed.append(out)
+        torch.cuda.synchronize()
+
+    assert len(calls) == g["cached_dit_calls"] and g["steps"] - len(calls) == g["cache_hits"]
+    kernels = [e for e in prof.key_averages() if "tfk::" in e.key]
+    assert sum(e.count for e in kernels) == 3 * g["cached_dit_calls"], [(e.key, e.count) for e in kernels]
+
+    bits = [tuple(to_host(t) for t in out) for out in handed]
+    for i, hit in enumerate(sched):
+        if hit:
+            assert handed[i] is handed[i - 1] or all(a is b for a, b in zip(handed[i], handed[i - 1]))
+            assert all(np.array_equal(a, b) for a, b in zip(bits[i], bits[i - 1])), f"step {i}"
+    for i in calls:
+        x, q, k, gu = (inputs[i][t] for t in ("x", "q", "k", "gate_up"))
+        y, qo, ko, o = bits[i]
+        check_close(y, oracle.rmsnorm_adaln_indexed(x, p["w"], p["shift"], p["scale"], idx, base.eps,
+                                                    threads=THREADS), f"step {i} a1")
+        rq, rk = oracle.qk_rmsnorm_rope_neox(q, k, p["w_q"], p["w_k"], pos, base.n_heads, base.head_dim,
+                                             base.theta, base.eps, threads=THREADS)
+        check_close(qo, rq.reshape(base.rows, -1), f"step {i} a2 q")
+        check_close(ko, rk.reshape(base.rows, -1), f"step {i} a2 k")
+        check_close(o, oracle.swiglu(gu, threads=THREADS), f"step {i} a3")
+    # consecutive DiT calls see different inputs, so a reused velocity is never a recomputation
+    assert not np.array_equal(bits[calls[0]][0], bits[calls[1]][0])
