@@ -68,7 +68,12 @@ int blocks_per_sm(const void* func, int threads, size_t smem) {
         const OccEntry& e = g_occ[i];
         if (e.dev == dev && e.func == func && e.threads == threads && e.smem == smem) return e.blocks;
     }
-    if (smem > 48 * 1024) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
+        cudaGetLastError();  // leave no stale error for the next launch check
+        return 0;
+    }
+    if (smem + fa.sharedSizeBytes > 48 * 1024) {  // beyond the default limit, static shared memory included
         // always the device maximum, so that launches of other sizes never lower it
         DeviceInfo di;
         if (g_have[dev].load(std::memory_order_acquire)) {
@@ -77,11 +82,6 @@ int blocks_per_sm(const void* func, int threads, size_t smem) {
             int optin = 0;
             if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
             di.max_smem_per_block_optin = optin;
-        }
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
-            cudaGetLastError();  // leave no stale error for the next launch check
-            return 0;
         }
         const int64_t dyn_max = (int64_t)di.max_smem_per_block_optin - (int64_t)fa.sharedSizeBytes;
         if ((int64_t)smem > dyn_max) return 0;
@@ -300,7 +300,7 @@ tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, t
     tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, padded_rows,
                      hidden, eps};
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return finish_launch(op, on_device(stream, [&] { return tfk::launch_rmsnorm_adaln(a, s); }));
+    return finish_launch(op, on_device(stream, [&] { return tfk::launch_rmsnorm_adaln(a, n_mod, s); }));
 }
 
 // sp_degree == 0: outputs are [padded_rows, out_row_stride] row layouts.

@@ -30,7 +30,7 @@ struct AdalnArgs {
     int hidden;
     float eps;
 };
-cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, cudaStream_t stream);
+cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, int n_mod, cudaStream_t stream);
 
 struct QkRopeArgs {
     const uint16_t* q;

@@ -272,6 +272,197 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     }
 }
 
+// ---- one warp per row --------------------------------------------------------
+//
+// A warp owns whole rows: lane l holds vectors l, l+32, ... of the row in
+// registers (VPL per lane), the sum of squares is one warp shuffle, and no
+// barrier or shared-memory exchange sits in the row loop at all.  A CTA owns a
+// contiguous run of rows and hands them to its warps in turn.  The modulation
+// of the rows it uses, mul = w * (1 + scale[m]) and add = shift[m], is
+// precombined into shared memory once, in four 16-byte planes per vector so
+// that the lanes of a warp read consecutive 16-byte words (no bank conflicts):
+//   tab[slot][plane][v], plane 0/1 = mul of elements 0-3 / 4-7, plane 2/3 = add.
+// Modulation row m may only use slot m % slots.  In a pass, each slot holds
+// the smallest m of the CTA's not yet computed rows that maps to it, and the
+// rows whose m is staged are computed; passes repeat until every row is done.
+// With at most `slots` modulation rows per CTA (every workload here) that is
+// one pass.  A row's arithmetic never depends on the slot, the pass or the
+// launch shape, so the output bits do not depend on how the rows are split
+// between CTAs or between calls.
+constexpr int kWarpMaxSlots = 64;
+constexpr int kNoRow = 0x7FFFFFFF;
+
+// Threads per CTA (one CTA per SM): the register budget of a thread is
+// 65536 / threads, and one row takes 4 * VPL registers of a lane.
+template <int VPL>
+constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? 768 : (VPL <= 16 ? 640 : 512));
+
+// RMSNorm + modulation of one row held in registers, stored to y.
+// t: the row's modulation slot in the shared table, offset by the lane.
+template <int VPL, bool kExact>
+__device__ __forceinline__ void warp_row_out(const AdalnArgs& a, int64_t row, int lane, int nvec, float inv_hidden,
+                                             const float4* t, const Vec8 (&xv)[VPL]) {
+    float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(xv[j].w[k] << 16), hi = __uint_as_float(xv[j].w[k] & 0xFFFF0000u);
+            ss0 = fmaf(lo, lo, ss0);
+            ss1 = fmaf(hi, hi, ss1);
+        }
+    }
+    const float inv_rms = rsqrtf(warp_sum(ss0 + ss1) * inv_hidden + a.eps);
+    const f32x2 r2 = f2_make(inv_rms, inv_rms);
+    // The output pass widens the bf16 words again, with byte permutes whose
+    // selectors carry a dependence on inv_rms (bit 16 and up of a selector is
+    // ignored, so the values are those of the plain widening).  Without it the
+    // compiler widened every word ahead, during the shuffles, and the widened
+    // row no longer fit in the register budget (spills).
+    const unsigned dep = (__float_as_uint(inv_rms) >> 31) << 16;
+    const unsigned sel_lo = 0x1044u | dep, sel_hi = 0x3244u | dep;
+    uint16_t* dst = a.y + row * a.y_stride + lane * 8;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+        if (!(kExact || j * 32 + lane < nvec)) continue;
+        const float4 m0 = t[j * 32], m1 = t[nvec + j * 32];
+        const float4 b0 = t[2 * nvec + j * 32], b1 = t[3 * nvec + j * 32];
+        f32x2 xw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            xw[k] = f2_make(__uint_as_float(__byte_perm(xv[j].w[k], 0u, sel_lo)),
+                            __uint_as_float(__byte_perm(xv[j].w[k], 0u, sel_hi)));
+        Vec8 o;
+        o.w[0] = f2_to_bf2(f2_fma(f2_mul(xw[0], r2), f2_make(m0.x, m0.y), f2_make(b0.x, b0.y)));
+        o.w[1] = f2_to_bf2(f2_fma(f2_mul(xw[1], r2), f2_make(m0.z, m0.w), f2_make(b0.z, b0.w)));
+        o.w[2] = f2_to_bf2(f2_fma(f2_mul(xw[2], r2), f2_make(m1.x, m1.y), f2_make(b1.x, b1.y)));
+        o.w[3] = f2_to_bf2(f2_fma(f2_mul(xw[3], r2), f2_make(m1.z, m1.w), f2_make(b1.z, b1.w)));
+        st_vec(dst + j * 256, o);
+    }
+}
+
+template <int VPL, bool kExact>
+__global__ void __launch_bounds__(kWarpThreads<VPL>, 1)
+rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float4* tab = reinterpret_cast<float4*>(smem_raw);  // [slots][4][nvec]
+    __shared__ int slot_m[kWarpMaxSlots];                // staged m per slot in this pass (kNoRow: none)
+    __shared__ int done_m[kWarpMaxSlots];                // rows with m <= done_m[m % slots] are computed
+    __shared__ int claimed_list[kWarpMaxSlots];
+    __shared__ int n_claimed;
+    __shared__ int more_passes;
+
+    const int nvec = a.hidden >> 3;
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = nt >> 5;
+    const float inv_hidden = 1.0f / (float)a.hidden;
+    const int64_t r0 = a.rows * (int64_t)blockIdx.x / gridDim.x;
+    const int64_t r1 = a.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
+
+    for (int s = tid; s < slots; s += nt) done_m[s] = -1;
+    grid_dep_wait();
+
+    // The next row of this warp after `r` whose modulation row is staged in
+    // this pass (r1 if none), and its slot.
+    auto next_staged = [&](int64_t r, int& slot) -> int64_t {
+        for (r += nwarps; r < r1; r += nwarps) {
+            const int m = __ldg(a.mod_idx + r);
+            slot = m % slots;
+            if (slot_m[slot] == m) return r;
+        }
+        return r1;
+    };
+
+    for (;;) {
+        for (int s = tid; s < slots; s += nt) slot_m[s] = kNoRow;
+        if (tid == 0) more_passes = 0;
+        __syncthreads();
+#pragma unroll 1
+        for (int64_t i = r0 + tid; i < r1; i += nt) {
+            const int m = __ldg(a.mod_idx + i);
+            if (m > done_m[m % slots]) atomicMin(&slot_m[m % slots], m);
+        }
+        __syncthreads();
+        // A row whose modulation row lost its slot needs another pass.
+        bool claimed = false, left = false;
+        for (int s = tid; s < slots; s += nt) claimed |= slot_m[s] != kNoRow;
+#pragma unroll 1
+        for (int64_t i = r0 + tid; i < r1; i += nt) {
+            const int m = __ldg(a.mod_idx + i);
+            left |= m > done_m[m % slots] && slot_m[m % slots] != m;
+        }
+        if (left) more_passes = 1;
+        if (tid == 0) {
+            int n = 0;
+            for (int s = 0; s < slots; ++s)
+                if (slot_m[s] != kNoRow) claimed_list[n++] = s;
+            n_claimed = n;
+        }
+        if (!__syncthreads_or(claimed)) break;  // uniform: every row is computed
+        const bool last_pass = more_passes == 0;
+
+
+        // The claimed modulation rows, staged as one flat loop over
+        // (slot, vector) so that all their loads are in flight together.
+        const int items = n_claimed * nvec;
+#pragma unroll 2
+        for (int it = tid; it < items; it += nt) {
+            const int s = claimed_list[it / nvec], v = it - (it / nvec) * nvec;
+            const int m = slot_m[s];
+            const float* srow = a.shift + (int64_t)m * a.hidden;
+            const float* crow = a.scale + (int64_t)m * a.hidden;
+            float4* t = tab + (int64_t)s * 4 * nvec;
+            const float4 w0 = ld_f4(a.weight + v * 8), w1 = ld_f4(a.weight + v * 8 + 4);
+            const float4 c0 = ld_f4(crow + v * 8), c1 = ld_f4(crow + v * 8 + 4);
+            const float4 b0 = ld_f4(srow + v * 8), b1 = ld_f4(srow + v * 8 + 4);
+            t[v] = make_float4(w0.x * (1.0f + c0.x), w0.y * (1.0f + c0.y), w0.z * (1.0f + c0.z), w0.w * (1.0f + c0.w));
+            t[nvec + v] = make_float4(w1.x * (1.0f + c1.x), w1.y * (1.0f + c1.y), w1.z * (1.0f + c1.z),
+                                      w1.w * (1.0f + c1.w));
+            t[2 * nvec + v] = b0;
+            t[3 * nvec + v] = b1;
+        }
+        __syncthreads();
+
+        int sa = 0;
+#pragma unroll 1
+        for (int64_t r = next_staged(r0 + warp - nwarps, sa); r < r1; r = next_staged(r, sa)) {
+            Vec8 xv[VPL];
+            const uint16_t* src = a.x + r * a.x_stride + lane * 8;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                if (kExact || j * 32 + lane < nvec) {
+                    xv[j] = ld_ro(src + j * 256);
+                } else {
+                    xv[j].w[0] = xv[j].w[1] = xv[j].w[2] = xv[j].w[3] = 0u;
+                }
+            }
+            warp_row_out<VPL, kExact>(a, r, lane, nvec, inv_hidden, tab + (int64_t)sa * 4 * nvec + lane, xv);
+        }
+        if (last_pass) break;  // uniform: no barrier needed after the last pass
+        __syncthreads();  // the next pass rewrites slot_m and the table
+        for (int s = tid; s < slots; s += nt)
+            if (slot_m[s] != kNoRow) done_m[s] = slot_m[s];
+    }
+
+    // Fixed-valid mode: this CTA's share of the padded tail is written +0.0.
+    const int64_t tail = a.padded_rows - a.rows;
+    if (tail > 0) {
+        const int64_t z0 = a.rows + tail * (int64_t)blockIdx.x / gridDim.x;
+        const int64_t z1 = a.rows + tail * (int64_t)(blockIdx.x + 1) / gridDim.x;
+        Vec8 zero;
+        zero.w[0] = zero.w[1] = zero.w[2] = zero.w[3] = 0u;
+        for (int64_t z = z0 + warp; z < z1; z += nwarps) {
+            uint16_t* dst = a.y + z * a.y_stride + lane * 8;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j)
+                if (kExact || j * 32 + lane < nvec) st_vec(dst + j * 256, zero);
+        }
+    }
+}
+
 // Two vectors per thread from hidden 512 on, four from 4096 (128-160
 // threads, a barrier over 4-5 warps: +2% at hidden 4096 and 5120 over two),
 // eight beyond 16384.  Short rows are issue-bound rather than memory-bound:
@@ -344,6 +535,76 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     return launch_kernel(rmsnorm_adaln_kernel<V, MAXT, kExact>, (unsigned)grid, threads, smem, stream, a, stages);
 }
 
+// The warp-per-row kernel takes the widths whose CTA-per-row shape keeps the
+// rows in their natural order (three whole vectors per thread, or four with
+// a ragged last thread), from 256 to 5120.  There a per-token change of
+// modulation row reloads the CTA's register-cached modulation on every
+// switch, while the warp kernel reads any staged row from shared memory.
+// Measured on the GB300 (event-timed launches, fraction of the measured copy
+// bandwidth, CTA kernel -> warp kernel):
+//   hidden 3072,  8,192 rows, 4 rows by modality and per-token coin flip: 0.48 -> 0.58
+//   hidden 3072, 30,358 rows, per-token coin flip between 2 rows:        0.64 -> 0.78
+//   hidden 4352, 30,000 rows, per-token coin flip:                        0.55 -> 0.81
+// and with long constant runs of one row the CTA kernel stays ahead by 1-3
+// points at these widths (3072 x 30,358: 0.81 vs 0.78), by 7-15 at the
+// widths that keep it (four whole vectors: 5120 0.96 vs 0.89, 4096 0.92
+// vs 0.78), where its row sort already handles alternating rows.
+#ifndef TFK_A1_WARP_MIN_HIDDEN
+#define TFK_A1_WARP_MIN_HIDDEN 256
+#endif
+#ifndef TFK_A1_WARP_MAX_HIDDEN
+#define TFK_A1_WARP_MAX_HIDDEN 5120
+#endif
+
+bool use_warp_kernel(int hidden) {
+    int v = 0, threads = 0;
+    if (hidden < 256 || hidden > 5120 || hidden < TFK_A1_WARP_MIN_HIDDEN || hidden > TFK_A1_WARP_MAX_HIDDEN ||
+        !choose_shape(hidden, &v, &threads))
+        return false;
+    const bool exact = 8 * v * threads == hidden;
+    return v == 3 || (v == 4 && !exact);
+}
+
+template <int VPL, bool kExact>
+cudaError_t launch_warp(const AdalnArgs& a, int n_mod, cudaStream_t stream) {
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    const int64_t slot_bytes = (int64_t)a.hidden * 8;
+    int64_t slots = ((int64_t)di.max_smem_per_block_optin - 2048) / slot_bytes;
+    if (slots > n_mod) slots = n_mod;
+    if (slots > kWarpMaxSlots) slots = kWarpMaxSlots;
+    if (slots < 1) slots = 1;
+    const size_t smem = (size_t)(slots * slot_bytes);
+    const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
+    // Few rows: smaller CTAs, so that the rows spread over all SMs.
+    int64_t warps = (work + di.sm_count - 1) / di.sm_count;
+    if (warps > kWarpThreads<VPL> / 32) warps = kWarpThreads<VPL> / 32;
+    if (warps < 1) warps = 1;
+    const int threads = (int)warps * 32;
+    const void* fn = reinterpret_cast<const void*>(&rmsnorm_adaln_warp_kernel<VPL, kExact>);
+    const int per_sm = blocks_per_sm(fn, threads, smem);
+    if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+    int64_t grid = (work + warps - 1) / warps;
+    if (grid > (int64_t)per_sm * di.sm_count) grid = (int64_t)per_sm * di.sm_count;
+    if (grid < 1) return cudaSuccess;
+    return launch_kernel(rmsnorm_adaln_warp_kernel<VPL, kExact>, (unsigned)grid, threads, smem, stream, a,
+                         (int)slots);
+}
+
+// Vectors per lane: the rows use_warp_kernel() admits have 192-640 vectors,
+// i.e. 6, 9, 12, 15 or 17-20 per lane.
+cudaError_t launch_warp_shape(const AdalnArgs& a, int n_mod, cudaStream_t stream) {
+    const int nvec = a.hidden / 8;
+    const int vpl = (nvec + 31) / 32;
+    const bool whole = nvec % 32 == 0;
+    if (vpl <= 6) return whole && vpl == 6 ? launch_warp<6, true>(a, n_mod, stream) : launch_warp<6, false>(a, n_mod, stream);
+    if (vpl <= 12)
+        return whole && vpl == 12 ? launch_warp<12, true>(a, n_mod, stream) : launch_warp<12, false>(a, n_mod, stream);
+    if (vpl <= 16) return launch_warp<16, false>(a, n_mod, stream);
+    return launch_warp<20, false>(a, n_mod, stream);
+}
+
 }  // namespace
 
 bool rmsnorm_adaln_supported(int hidden) {
@@ -351,7 +612,8 @@ bool rmsnorm_adaln_supported(int hidden) {
     return hidden > 0 && hidden % 8 == 0 && choose_shape(hidden, &v, &t);
 }
 
-cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, cudaStream_t stream) {
+cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, int n_mod, cudaStream_t stream) {
+    if (use_warp_kernel(a.hidden)) return launch_warp_shape(a, n_mod, stream);
     int v = 0, threads = 0;
     if (!choose_shape(a.hidden, &v, &threads)) return cudaErrorInvalidValue;
     const bool exact = 8 * v * threads == a.hidden;
