@@ -180,7 +180,8 @@ class ClockSampler:
 
 
 def profiled_traffic(kernel: str, workload: str, source: str) -> float | None:
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    """DRAM bytes per launch of `kernel` from the committed ncu summary (a capture of a
+    16,384-token prefix scaled to the full workload, profiles/dram_traffic.txt), if it was
     taken on the kernel source as it is now (sha256 of the .cu file)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
@@ -590,7 +591,11 @@ def run_tfk(args, ranks: Ranks) -> dict | None:
     src = {"rmsnorm_adaln": "rmsnorm_adaln.cu", "qk_rmsnorm_rope": "qk_rmsnorm_rope.cu", "swiglu": "swiglu.cu"}
     roofline = {"bound": "hbm", "kernel": dom_name, "achieved": kernels[dom_name]["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": kernels[dom_name]["frac"],
-                "traffic": profiled_traffic(dom_name, wl.name, src[dom_name]),
+                "traffic": profiled_traffic(dom_name, wl.name, src[dom_name]) if wl.rows == synth.get(wl.name).rows
+                else None,
+                "traffic_source": "ncu DRAM bytes of a 16,384-token prefix launch, reads scaled by rows, writes "
+                                  "= full algorithmic writes minus the L2-resident remainder "
+                                  "(profiles/dram_traffic.txt)",
                 "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peaks["source"] == "measured" else "fallback 6.8 TB/s",
                 "bytes_per_launch": chain.bytes[dom], "ms_per_launch": per_kernel[dom]}
