@@ -99,11 +99,11 @@ int blocks_per_sm(const void* func, int threads, size_t smem) {
     return blocks;
 }
 
-int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes) {
+int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes, int inflight_per_sm) {
     DeviceInfo di;
     if (device_info(&di) != cudaSuccess || stage_bytes <= 0) return 2;
     if (ctas_per_sm < 1) ctas_per_sm = 1;
-    int ahead = (kInflightPerSm + ctas_per_sm * stage_bytes - 1) / (ctas_per_sm * stage_bytes);
+    int ahead = (inflight_per_sm + ctas_per_sm * stage_bytes - 1) / (ctas_per_sm * stage_bytes);
     int stages = ahead + 1;
     if (stages > 16) stages = 16;
     // shared memory per SM (1 KB reserved per CTA) and per CTA (1 KB left for static shared memory)

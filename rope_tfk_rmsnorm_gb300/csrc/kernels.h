@@ -79,14 +79,14 @@ bool qk_rope_supported(int n_heads, int head_dim);
 int blocks_per_sm(const void* func, int threads, size_t smem_bytes);
 
 // Depth of a cp.async staging ring (2..16 stages of `stage_bytes`) that keeps
-// about kInflightPerSm bytes in flight per SM when `ctas_per_sm` CTAs share
+// about `inflight_per_sm` bytes in flight per SM when `ctas_per_sm` CTAs share
 // an SM, within the shared memory of the SM and of one CTA (`extra_bytes` of
 // other dynamic shared memory per CTA).
 #ifndef TFK_INFLIGHT_KB
 #define TFK_INFLIGHT_KB 112
 #endif
 constexpr int kInflightPerSm = TFK_INFLIGHT_KB * 1024;
-int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes);
+int pick_stages(int ctas_per_sm, int stage_bytes, int extra_bytes, int inflight_per_sm = kInflightPerSm);
 
 // Programmatic dependent launch: a kernel of this library may be scheduled
 // while the previous kernel on its stream drains its last CTAs.  Each kernel

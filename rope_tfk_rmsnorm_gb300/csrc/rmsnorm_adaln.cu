@@ -295,7 +295,7 @@ constexpr int kNoRow = 0x7FFFFFFF;
 // Threads per CTA (one CTA per SM): the register budget of a thread is
 // 65536 / threads, and one row takes 4 * VPL registers of a lane.
 template <int VPL>
-constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? 768 : (VPL <= 16 ? 640 : 512));
+constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? 768 : (VPL <= 16 ? 640 : (VPL <= 20 ? 512 : 448)));
 
 // RMSNorm + modulation of one row held in registers, stored to y.
 // t: the row's modulation slot in the shared table, offset by the lane.
@@ -519,7 +519,10 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     const void* fn = reinterpret_cast<const void*>(&rmsnorm_adaln_kernel<V, MAXT, kExact>);
     const int by_regs = blocks_per_sm(fn, threads, 0);
     if (by_regs <= 0) return cudaErrorInvalidConfiguration;
-    const int stages = pick_stages(by_regs, row_bytes, 0);
+    // Rows of 16 KB and more (hidden >= 8192) keep 80 KB in flight per SM
+    // instead of 112: measured +1.5-2 points at hidden 12288 and 16384 (the
+    // ring then takes fewer of the SM's 228 KB of shared memory).
+    const int stages = pick_stages(by_regs, row_bytes, 0, row_bytes >= 16384 ? 80 * 1024 : kInflightPerSm);
     const size_t smem = (size_t)stages * row_bytes;
     const int per_sm = blocks_per_sm(fn, threads, smem);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
@@ -553,12 +556,12 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
 #define TFK_A1_WARP_MIN_HIDDEN 256
 #endif
 #ifndef TFK_A1_WARP_MAX_HIDDEN
-#define TFK_A1_WARP_MAX_HIDDEN 5120
+#define TFK_A1_WARP_MAX_HIDDEN 6144
 #endif
 
 bool use_warp_kernel(int hidden) {
     int v = 0, threads = 0;
-    if (hidden < 256 || hidden > 5120 || hidden < TFK_A1_WARP_MIN_HIDDEN || hidden > TFK_A1_WARP_MAX_HIDDEN ||
+    if (hidden < 256 || hidden > 6144 || hidden < TFK_A1_WARP_MIN_HIDDEN || hidden > TFK_A1_WARP_MAX_HIDDEN ||
         !choose_shape(hidden, &v, &threads))
         return false;
     const bool exact = 8 * v * threads == hidden;
@@ -602,7 +605,8 @@ cudaError_t launch_warp_shape(const AdalnArgs& a, int n_mod, cudaStream_t stream
     if (vpl <= 12)
         return whole && vpl == 12 ? launch_warp<12, true>(a, n_mod, stream) : launch_warp<12, false>(a, n_mod, stream);
     if (vpl <= 16) return launch_warp<16, false>(a, n_mod, stream);
-    return launch_warp<20, false>(a, n_mod, stream);
+    if (vpl <= 20) return launch_warp<20, false>(a, n_mod, stream);
+    return whole && vpl == 24 ? launch_warp<24, true>(a, n_mod, stream) : launch_warp<24, false>(a, n_mod, stream);
 }
 
 }  // namespace

@@ -141,6 +141,11 @@ ADALN_CASES = [
     (64, 16384, 3, "random"),
     (17, 32768, 2, "random"),        # largest hidden
     (2500, 512, 28, "blocks"),
+    (301, 4352, 3, "random"),        # warp-per-row kernel: 17 of 20 vectors per lane
+    (257, 5632, 2, "random"),        # 22 of 24 vectors per lane
+    (130, 6144, 3, "pairs"),         # 24 whole vectors per lane
+    (4560, 2304, 70, "random"),      # 30 rows per CTA over more modulation rows than slots: several passes
+    (77, 12288, 2, "random"),        # 80 KB in flight per SM for rows of 16 KB and more
 ]
 
 
