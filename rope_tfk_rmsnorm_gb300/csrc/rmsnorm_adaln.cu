@@ -294,8 +294,16 @@ constexpr int kNoRow = 0x7FFFFFFF;
 
 // Threads per CTA (one CTA per SM): the register budget of a thread is
 // 65536 / threads, and one row takes 4 * VPL registers of a lane.
+#ifndef TFK_A1_WT12
+#define TFK_A1_WT12 768
+#endif
+#ifndef TFK_A1_WMINB
+#define TFK_A1_WMINB 1
+#endif
 template <int VPL>
-constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? 768 : (VPL <= 16 ? 640 : (VPL <= 20 ? 512 : 448)));
+constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? TFK_A1_WT12 : (VPL <= 16 ? 640 : (VPL <= 20 ? 512 : 448)));
+template <int VPL>
+constexpr int kWarpMinBlocks = VPL <= 4 ? 1 : (VPL <= 12 ? TFK_A1_WMINB : 1);
 
 // RMSNorm + modulation of one row held in registers, stored to y.
 // t: the row's modulation slot in the shared table, offset by the lane.
@@ -342,7 +350,7 @@ __device__ __forceinline__ void warp_row_out(const AdalnArgs& a, int64_t row, in
 }
 
 template <int VPL, bool kExact>
-__global__ void __launch_bounds__(kWarpThreads<VPL>, 1)
+__global__ void __launch_bounds__(kWarpThreads<VPL>, kWarpMinBlocks<VPL>)
 rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float4* tab = reinterpret_cast<float4*>(smem_raw);  // [slots][4][nvec]

@@ -2,7 +2,8 @@
 
 The launchers pick among many kernel instantiations by shape: one, two,
 three, four or eight vectors per thread (whole-vector widths without bounds
-predicates) for RMSNorm+AdaLN; one to four heads per lane group, masked last
+predicates) or one warp per row (6 to 24 vectors per lane, staged modulation
+rows in one or several passes) for RMSNorm+AdaLN; one to four heads per lane group, masked last
 groups and side-by-side token streams for Q/K; one chunk per CTA or several
 whole rows for SwiGLU; 4-row tiles or the column walk for the relayouts.
 Every case here draws its shape from a fixed seed, so a wrong choice or a bad
@@ -69,7 +70,23 @@ def _ulysses_cases(n):
     return out
 
 
+def _adaln_warp_cases(n):
+    """Widths of the warp-per-row RMSNorm kernel (multiples of 768 from 1536 to 6144, and the
+    widths between 4096 and 6144 that are not multiples of 1024) at row counts that fill
+    several warps per CTA, with up to 90 modulation rows drawn per token, so that a CTA's rows
+    may need more modulation rows than fit in shared memory (several passes)."""
+    whole = [768 * k for k in range(2, 9)]
+    ragged = [h for h in range(4104, 6144, 8) if h % 1024]
+    out = []
+    for i in range(n):
+        hidden = int(_RNG.choice(whole if i % 2 == 0 else ragged))
+        rows = int(_RNG.integers(300, max(301, min(12000, 24_000_000 // hidden))))
+        out.append((rows, hidden, int(_RNG.integers(1, 91)), int(_RNG.integers(0, 2 ** 31))))
+    return out
+
+
 ADALN = _adaln_cases(40)
+ADALN_WARP = _adaln_warp_cases(10)
 QK = _qk_cases(40)
 SWIGLU = _swiglu_cases(20)
 ULYSSES = _ulysses_cases(16)
@@ -78,6 +95,17 @@ ULYSSES = _ulysses_cases(16)
 @pytest.mark.parametrize("rows,hidden,n_mod,seed", ADALN,
                          ids=[f"{r}x{h}m{m}" for r, h, m, _ in ADALN])
 def test_adaln_random_shapes(cuda, rows, hidden, n_mod, seed):
+    rng = np.random.default_rng(seed)
+    x = rand_bits(rng, (rows, hidden), 2.0)
+    w, sh, sc = mod_params(rng, n_mod, hidden)
+    idx = rng.integers(0, n_mod, rows).astype(np.int32)
+    check_close(gpu_adaln(x, w, sh, sc, idx, 1e-6), ora_adaln(x, w, sh, sc, idx, 1e-6),
+                f"a1 {rows}x{hidden}")
+
+
+@pytest.mark.parametrize("rows,hidden,n_mod,seed", ADALN_WARP,
+                         ids=[f"{r}x{h}m{m}" for r, h, m, _ in ADALN_WARP])
+def test_adaln_warp_kernel_random_shapes(cuda, rows, hidden, n_mod, seed):
     rng = np.random.default_rng(seed)
     x = rand_bits(rng, (rows, hidden), 2.0)
     w, sh, sc = mod_params(rng, n_mod, hidden)
