@@ -161,6 +161,29 @@ __device__ __forceinline__ Vec8 ld_smem_vec(const void* p) {
     return v;
 }
 
+// ---- thread-block clusters ---------------------------------------------------
+
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (a hardware
+// barrier, like __syncthreads for the cluster); shared-memory writes made
+// before it, to this CTA or to another CTA of the cluster, are visible after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v to the same shared-memory variable as `local` in CTA `peer` of the cluster.
+__device__ __forceinline__ void st_peer_f32(const void* local, unsigned peer, float v) {
+    unsigned remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(peer));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
+}
+
 // ---- reductions -------------------------------------------------------------
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -89,15 +89,38 @@ template <int V, int MAXT, bool kExact>
 constexpr int kMinBlocks = V == 1 ? 2 : (V == 2 ? (MAXT <= 256 && kExact ? 3 : 2 * (512 / MAXT))
                                                 : (V == 3 ? 3 : 1));
 
-template <int V, int MAXT, bool kExact>
+// kPair: a cluster of two CTAs shares each row, for rows too wide for one CTA
+// to hold the modulation of its columns in registers (hidden > 16384).  CTA c
+// of the pair takes the columns of vectors [c * half, ...) (half = the first
+// ceil(nvec / 2) vectors), both run the pair's rows in the same order, and
+// per row each adds the other's partial sum of squares, exchanged through
+// distributed shared memory with one cluster barrier; both then form the same
+// total, partial(CTA 0) + partial(CTA 1).
+template <int V, int MAXT, bool kExact, bool kPair = false>
 __global__ void __launch_bounds__(MAXT, (kMinBlocks<V, MAXT, kExact>))
-rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
+rmsnorm_adaln_kernel(const AdalnArgs args, const int stages) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Vec8* ring = reinterpret_cast<Vec8*>(smem_raw);  // [stages][nvec]
     __shared__ float partial[2][32];
+    __shared__ float xchg[2][2];  // [row parity][CTA of the pair]: partial sums (kPair)
     grid_dep_wait();
 
-    const int nvec = a.hidden >> 3;
+    const unsigned crank = kPair ? cluster_ctarank() : 0u;
+    const int half = ((args.hidden >> 3) + 1) >> 1;
+    // vectors of this CTA's columns
+    const int nvec = !kPair ? args.hidden >> 3 : (crank ? (args.hidden >> 3) - half : half);
+    const unsigned unit = kPair ? blockIdx.x >> 1 : blockIdx.x;
+    const unsigned units = kPair ? gridDim.x >> 1 : gridDim.x;
+    AdalnArgs half_args = args;  // kPair: the arguments moved to this CTA's columns
+    if constexpr (kPair) {
+        const int cbase = crank ? half : 0;
+        half_args.x += cbase * 8;
+        half_args.y += cbase * 8;
+        half_args.weight += cbase * 8;
+        half_args.shift += cbase * 8;
+        half_args.scale += cbase * 8;
+    }
+    const AdalnArgs& a = kPair ? half_args : args;
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
     const int lane = tid & 31;
@@ -105,8 +128,8 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     const int nwarps = (nt + 31) >> 5;
     const float inv_hidden = 1.0f / (float)a.hidden;
 
-    const int64_t r0 = a.rows * (int64_t)blockIdx.x / gridDim.x;
-    const int64_t r1 = a.rows * (int64_t)(blockIdx.x + 1) / gridDim.x;
+    const int64_t r0 = a.rows * (int64_t)unit / units;
+    const int64_t r1 = a.rows * (int64_t)(unit + 1) / units;
     const int nrows = (int)(r1 - r0);
 
     int col[V];
@@ -237,7 +260,15 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
             }
 
             __syncthreads();
-            const float total = warp_sum(lane < nwarps ? partial[it & 1][lane] : 0.f);
+            float total = warp_sum(lane < nwarps ? partial[it & 1][lane] : 0.f);
+            if constexpr (kPair) {
+                if (tid == 0) {
+                    xchg[it & 1][crank] = total;
+                    st_peer_f32(&xchg[it & 1][crank], crank ^ 1u, total);
+                }
+                cluster_sync();  // both partials of this row are in both CTAs
+                total = xchg[it & 1][0] + xchg[it & 1][1];
+            }
             const float inv_rms = rsqrtf(total * inv_hidden + a.eps);
 
             uint16_t* dst = a.y + r * a.y_stride;
@@ -259,8 +290,8 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
     // in the same launch (stores only; the tail of x is never read).
     const int64_t tail = a.padded_rows - a.rows;
     if (tail > 0) {
-        const int64_t z0 = a.rows + tail * (int64_t)blockIdx.x / gridDim.x;
-        const int64_t z1 = a.rows + tail * (int64_t)(blockIdx.x + 1) / gridDim.x;
+        const int64_t z0 = a.rows + tail * (int64_t)unit / units;
+        const int64_t z1 = a.rows + tail * (int64_t)(unit + 1) / units;
         Vec8 zero;
         zero.w[0] = zero.w[1] = zero.w[2] = zero.w[3] = 0u;
         for (int64_t r = z0; r < z1; ++r) {
@@ -270,6 +301,8 @@ rmsnorm_adaln_kernel(const AdalnArgs a, const int stages) {
                 if (ok[i]) st_vec(dst + col[i] * 8, zero);
         }
     }
+    // No CTA of a pair leaves while the other may still write to its shared memory.
+    if constexpr (kPair) cluster_sync();
 }
 
 // ---- one warp per row --------------------------------------------------------
@@ -617,6 +650,45 @@ cudaError_t launch_warp_shape(const AdalnArgs& a, int n_mod, cudaStream_t stream
     return whole && vpl == 24 ? launch_warp<24, true>(a, n_mod, stream) : launch_warp<24, false>(a, n_mod, stream);
 }
 
+// Rows of more than 2176 vectors (hidden 17416 and wider): a pair of CTAs per
+// row, each with the four-vector shape on its half (at most 2048 vectors, 512
+// threads).  Measured against eight vectors per thread in one CTA, which spill
+// (fraction of the copy bandwidth, 10,000 rows, event-timed): 18432 0.33 ->
+// 0.39, 20480 0.35 -> 0.42, 24576 0.40 -> 0.45, 32768 0.46 -> 0.49; at 16392
+// and 17408 the single CTA stays ahead (0.30 vs 0.28, 0.32 vs 0.30).  What
+// holds the pairs back is the per-row cluster barrier: its release waits for
+// the arriving threads' earlier memory operations, and the same kernel with
+// a relaxed arrive (which does not make the exchanged sums visible, so a
+// measurement only) ran at 0.63 at 20480 and 0.72 at 32768.
+#ifndef TFK_A1_PAIR_FROM_NVEC
+#define TFK_A1_PAIR_FROM_NVEC 2176
+#endif
+template <bool kExact>
+cudaError_t launch_pair(const AdalnArgs& a, int threads, cudaStream_t stream) {
+    DeviceInfo di;
+    cudaError_t err = device_info(&di);
+    if (err != cudaSuccess) return err;
+    const int half = (a.hidden / 8 + 1) / 2;
+    const int row_bytes = half * 16;
+    auto kern = rmsnorm_adaln_kernel<4, kMaxThreads, kExact, true>;
+    const void* fn = reinterpret_cast<const void*>(kern);
+    const int by_regs = blocks_per_sm(fn, threads, 0);
+    if (by_regs <= 0) return cudaErrorInvalidConfiguration;
+    const int stages = pick_stages(by_regs, row_bytes, 0, row_bytes >= 16384 ? 80 * 1024 : kInflightPerSm);
+    const size_t smem = (size_t)stages * row_bytes;
+    const int per_sm = blocks_per_sm(fn, threads, smem);
+    if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+    int64_t pairs = (int64_t)per_sm * di.sm_count / 2;
+    if (pairs < 1) pairs = 1;
+    const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
+    const int64_t chunks = (work + kRowsPerCta - 1) / kRowsPerCta;
+    if (chunks > pairs && work >= kChunkMinRun * pairs) pairs = chunks;
+    if (pairs > (1 << 23)) pairs = 1 << 23;
+    if (pairs > work) pairs = work;
+    if (pairs < 1) return cudaSuccess;
+    return launch_kernel_cluster(kern, (unsigned)(2 * pairs), threads, smem, 2, stream, a, stages);
+}
+
 }  // namespace
 
 bool rmsnorm_adaln_supported(int hidden) {
@@ -626,6 +698,13 @@ bool rmsnorm_adaln_supported(int hidden) {
 
 cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, int n_mod, cudaStream_t stream) {
     if (use_warp_kernel(a.hidden)) return launch_warp_shape(a, n_mod, stream);
+    const int nvec = a.hidden / 8;
+    if (nvec > TFK_A1_PAIR_FROM_NVEC) {
+        const int half = (nvec + 1) / 2;
+        const int threads = ((half + 3) / 4 + 31) / 32 * 32;
+        const bool exact = nvec % 2 == 0 && 4 * threads == half;
+        return exact ? launch_pair<true>(a, threads, stream) : launch_pair<false>(a, threads, stream);
+    }
     int v = 0, threads = 0;
     if (!choose_shape(a.hidden, &v, &threads)) return cudaErrorInvalidValue;
     const bool exact = 8 * v * threads == a.hidden;

@@ -146,6 +146,10 @@ ADALN_CASES = [
     (130, 6144, 3, "pairs"),         # 24 whole vectors per lane
     (4560, 2304, 70, "random"),      # 30 rows per CTA over more modulation rows than slots: several passes
     (77, 12288, 2, "random"),        # 80 KB in flight per SM for rows of 16 KB and more
+    (40, 16392, 3, "random"),        # eight vectors per thread, one CTA per row
+    (29, 17416, 3, "random"),        # a pair of CTAs per row: halves of 1089 and 1088 vectors
+    (33, 20480, 2, "pairs"),         # pair: 1280 whole vectors per CTA
+    (200, 24576, 4, "random"),
 ]
 
 
@@ -491,7 +495,7 @@ def _full_chain(wl):
     return out
 
 
-@pytest.mark.parametrize("rows,hidden", [(120000, 512), (50000, 3072), (20000, 16384)])
+@pytest.mark.parametrize("rows,hidden", [(120000, 512), (50000, 3072), (20000, 16384), (12000, 20480)])
 def test_adaln_chunked_schedule_sampled(cuda, rows, hidden):
     """One, two and eight vectors per thread at row counts where the RMSNorm
     kernel hands out 24-row chunks instead of one persistent run per CTA (more
@@ -587,6 +591,26 @@ def test_fixed_valid_adaln_and_qk(cuda, N, L, H):
     rq, rk = oracle.qk_rmsnorm_rope_neox_fixed_valid(q, k, L, wq, wk, pos, H, D, 10000.0, 1e-6, threads=THREADS)
     check_close(qo.host(), rq.reshape(N, -1), "fixed-valid q")
     check_close(ko.host(), rk.reshape(N, -1), "fixed-valid k")
+
+
+@pytest.mark.parametrize("N,L,hidden", [(500, 333, 20480), (300, 300, 6144), (257, 0, 32768)])
+def test_fixed_valid_adaln_wide_rows(cuda, N, L, hidden):
+    """Fixed-valid RMSNorm+AdaLN on the wide-row paths (a pair of CTAs per row; the warp
+    kernel at 6144): valid rows against the oracle, the tail +0.0, NaN tail never read."""
+    rng = np.random.default_rng(N + L + hidden)
+    x = rand_bits(rng, (N, hidden))
+    x[L:] = synth.BF16_NAN
+    w, sh, sc = mod_params(rng, 3, hidden)
+    idx = rng.integers(0, 3, L).astype(np.int32)
+    y = Guarded(N, hidden)
+    tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(to_dev(x), L, f32_dev(w), f32_dev(sh), f32_dev(sc), i32_dev(idx),
+                                              1e-6, out=y.view)
+    torch.cuda.synchronize()
+    y.check()
+    got = y.host()
+    assert np.all(got[L:] == 0x0000)
+    check_close(got, oracle.rmsnorm_adaln_fixed_valid(x, L, w, sh, sc, idx, 1e-6, threads=THREADS),
+                f"fixed-valid a1 hidden {hidden}")
 
 
 def test_fixed_valid_in_place_on_the_valid_only_workload(cuda):
