@@ -315,11 +315,12 @@ rmsnorm_adaln_kernel(const AdalnArgs args, const int stages) {
 // precombined into shared memory once, in four 16-byte planes per vector so
 // that the lanes of a warp read consecutive 16-byte words (no bank conflicts):
 //   tab[slot][plane][v], plane 0/1 = mul of elements 0-3 / 4-7, plane 2/3 = add.
-// Modulation row m may only use slot m % slots.  In a pass, each slot holds
-// the smallest m of the CTA's not yet computed rows that maps to it, and the
-// rows whose m is staged are computed; passes repeat until every row is done.
-// With at most `slots` modulation rows per CTA (every workload here) that is
-// one pass.  A row's arithmetic never depends on the slot, the pass or the
+// Modulation row m may only use slot m % slots.  When every modulation row
+// has a slot (n_mod <= slots, as in every workload here), the CTA stages them
+// all in one pass without reading the indices first.  Otherwise, in a pass,
+// each slot holds the smallest m of the CTA's not yet computed rows that maps
+// to it, and the rows whose m is staged are computed; passes repeat until
+// every row is done (one pass when the CTA's rows use at most `slots` rows).  A row's arithmetic never depends on the slot, the pass or the
 // launch shape, so the output bits do not depend on how the rows are split
 // between CTAs or between calls.
 constexpr int kWarpMaxSlots = 64;
@@ -384,7 +385,7 @@ __device__ __forceinline__ void warp_row_out(const AdalnArgs& a, int64_t row, in
 
 template <int VPL, bool kExact>
 __global__ void __launch_bounds__(kWarpThreads<VPL>, kWarpMinBlocks<VPL>)
-rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots) {
+rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots, const int n_mod) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float4* tab = reinterpret_cast<float4*>(smem_raw);  // [slots][4][nvec]
     __shared__ int slot_m[kWarpMaxSlots];                // staged m per slot in this pass (kNoRow: none)
@@ -418,32 +419,44 @@ rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots) {
     };
 
     for (;;) {
-        for (int s = tid; s < slots; s += nt) slot_m[s] = kNoRow;
-        if (tid == 0) more_passes = 0;
-        __syncthreads();
+        bool last_pass = true;
+        if (slots >= n_mod) {
+            // Every modulation row has a slot of its own (m % slots == m): one
+            // pass that stages all of them, without reading the indices first.
+            for (int s = tid; s < slots; s += nt) {
+                slot_m[s] = s;
+                claimed_list[s] = s;
+            }
+            if (tid == 0) n_claimed = slots;
+            __syncthreads();
+        } else {
+            for (int s = tid; s < slots; s += nt) slot_m[s] = kNoRow;
+            if (tid == 0) more_passes = 0;
+            __syncthreads();
 #pragma unroll 1
-        for (int64_t i = r0 + tid; i < r1; i += nt) {
-            const int m = __ldg(a.mod_idx + i);
-            if (m > done_m[m % slots]) atomicMin(&slot_m[m % slots], m);
-        }
-        __syncthreads();
-        // A row whose modulation row lost its slot needs another pass.
-        bool claimed = false, left = false;
-        for (int s = tid; s < slots; s += nt) claimed |= slot_m[s] != kNoRow;
+            for (int64_t i = r0 + tid; i < r1; i += nt) {
+                const int m = __ldg(a.mod_idx + i);
+                if (m > done_m[m % slots]) atomicMin(&slot_m[m % slots], m);
+            }
+            __syncthreads();
+            // A row whose modulation row lost its slot needs another pass.
+            bool claimed = false, left = false;
+            for (int s = tid; s < slots; s += nt) claimed |= slot_m[s] != kNoRow;
 #pragma unroll 1
-        for (int64_t i = r0 + tid; i < r1; i += nt) {
-            const int m = __ldg(a.mod_idx + i);
-            left |= m > done_m[m % slots] && slot_m[m % slots] != m;
+            for (int64_t i = r0 + tid; i < r1; i += nt) {
+                const int m = __ldg(a.mod_idx + i);
+                left |= m > done_m[m % slots] && slot_m[m % slots] != m;
+            }
+            if (left) more_passes = 1;
+            if (tid == 0) {
+                int n = 0;
+                for (int s = 0; s < slots; ++s)
+                    if (slot_m[s] != kNoRow) claimed_list[n++] = s;
+                n_claimed = n;
+            }
+            if (!__syncthreads_or(claimed)) break;  // uniform: every row is computed
+            last_pass = more_passes == 0;
         }
-        if (left) more_passes = 1;
-        if (tid == 0) {
-            int n = 0;
-            for (int s = 0; s < slots; ++s)
-                if (slot_m[s] != kNoRow) claimed_list[n++] = s;
-            n_claimed = n;
-        }
-        if (!__syncthreads_or(claimed)) break;  // uniform: every row is computed
-        const bool last_pass = more_passes == 0;
 
 
         // The claimed modulation rows, staged as one flat loop over
@@ -633,7 +646,7 @@ cudaError_t launch_warp(const AdalnArgs& a, int n_mod, cudaStream_t stream) {
     if (grid > (int64_t)per_sm * di.sm_count) grid = (int64_t)per_sm * di.sm_count;
     if (grid < 1) return cudaSuccess;
     return launch_kernel(rmsnorm_adaln_warp_kernel<VPL, kExact>, (unsigned)grid, threads, smem, stream, a,
-                         (int)slots);
+                         (int)slots, n_mod);
 }
 
 // Vectors per lane: the rows use_warp_kernel() admits have 192-640 vectors,
