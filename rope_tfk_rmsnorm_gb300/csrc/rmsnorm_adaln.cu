@@ -5,7 +5,17 @@
 // per-token indexed AdaLN modulation; TeleFuser PR #23, section Changes
 // Made: the indexed-modulation kernel.
 //
-// Design (HBM-bound: 2 bytes read + 2 bytes written per element):
+// Three kernels, chosen by hidden alone (so a row's output bits never depend
+// on the rows of the call):
+// - rmsnorm_adaln_kernel, one CTA per row (below);
+// - the same kernel in pairs (kPair): a cluster of two CTAs per row, each with
+//   half the columns, for rows wider than 17408;
+// - rmsnorm_adaln_warp_kernel, one warp per row with the modulation staged in
+//   shared memory, for the widths where the CTA shape keeps rows unsorted
+//   (see "one warp per row" below).
+//
+// Design of the CTA-per-row kernel (HBM-bound: 2 bytes read + 2 bytes written
+// per element):
 // - Persistent CTAs, each owning a contiguous run of rows, so the modulation
 //   index changes rarely inside a CTA in the packed video+audio layout.
 // - Each thread owns the same 8*V columns of every row.  The norm weight for
@@ -320,24 +330,19 @@ rmsnorm_adaln_kernel(const AdalnArgs args, const int stages) {
 // all in one pass without reading the indices first.  Otherwise, in a pass,
 // each slot holds the smallest m of the CTA's not yet computed rows that maps
 // to it, and the rows whose m is staged are computed; passes repeat until
-// every row is done (one pass when the CTA's rows use at most `slots` rows).  A row's arithmetic never depends on the slot, the pass or the
-// launch shape, so the output bits do not depend on how the rows are split
-// between CTAs or between calls.
+// every row is done (one pass when the CTA's rows use at most `slots` rows).
+// A row's arithmetic never depends on the slot, the pass or the launch shape,
+// so the output bits do not depend on how the rows are split between CTAs or
+// between calls.
 constexpr int kWarpMaxSlots = 64;
 constexpr int kNoRow = 0x7FFFFFFF;
 
 // Threads per CTA (one CTA per SM): the register budget of a thread is
-// 65536 / threads, and one row takes 4 * VPL registers of a lane.
-#ifndef TFK_A1_WT12
-#define TFK_A1_WT12 768
-#endif
-#ifndef TFK_A1_WMINB
-#define TFK_A1_WMINB 1
-#endif
+// 65536 / threads, and one row takes 4 * VPL registers of a lane.  Measured at
+// 12 vectors per lane: 768 threads and 640 equal; three CTAs of 256 or two of
+// 384 per SM 1-4 points lower.
 template <int VPL>
-constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? TFK_A1_WT12 : (VPL <= 16 ? 640 : (VPL <= 20 ? 512 : 448)));
-template <int VPL>
-constexpr int kWarpMinBlocks = VPL <= 4 ? 1 : (VPL <= 12 ? TFK_A1_WMINB : 1);
+constexpr int kWarpThreads = VPL <= 4 ? 1024 : (VPL <= 12 ? 768 : (VPL <= 16 ? 640 : (VPL <= 20 ? 512 : 448)));
 
 // RMSNorm + modulation of one row held in registers, stored to y.
 // t: the row's modulation slot in the shared table, offset by the lane.
@@ -384,7 +389,7 @@ __device__ __forceinline__ void warp_row_out(const AdalnArgs& a, int64_t row, in
 }
 
 template <int VPL, bool kExact>
-__global__ void __launch_bounds__(kWarpThreads<VPL>, kWarpMinBlocks<VPL>)
+__global__ void __launch_bounds__(kWarpThreads<VPL>, 1)
 rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots, const int n_mod) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float4* tab = reinterpret_cast<float4*>(smem_raw);  // [slots][4][nvec]
