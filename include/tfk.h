@@ -50,7 +50,13 @@ typedef enum {
 
 typedef uint16_t tfk_bf16; /* raw bf16 bits */
 
-#define TFK_ABI_VERSION 1
+#define TFK_ABI_VERSION 2
+
+/*
+ * Bytes of the optional device workspace of the two RMSNorm+AdaLN entry
+ * points (row counters for dynamic scheduling; see tfk_rmsnorm_adaln_indexed).
+ */
+#define TFK_RMSNORM_WORKSPACE_BYTES 2304
 
 /* ABI version of the loaded library (TFK_ABI_VERSION at build time). */
 int tfk_abi_version(void);
@@ -85,12 +91,24 @@ tfk_status tfk_debug_fail_next_launch(int32_t cuda_error);
  * shift, scale  [n_mod, hidden] fp32 modulation rows (row-major, contiguous).
  * mod_idx [rows] int32, 0 <= mod_idx[t] < n_mod (precondition).
  * hidden  multiple of 8, 8 <= hidden <= 32768.  eps >= 0.
+ * workspace  optional DEVICE memory of TFK_RMSNORM_WORKSPACE_BYTES bytes,
+ *         8-byte aligned, owned by the caller, or NULL.  With it, the kernels
+ *         that keep the rows' modulation in shared memory hand rows to warps
+ *         as they become free (a row counter in the workspace) instead of
+ *         splitting the rows evenly up front, which keeps every SM busy to
+ *         the end; the output bits are the same either way.  It must be zero
+ *         before its first use; every call that completes leaves it zero.
+ *         Calls that may run at the same time on the GPU (other streams,
+ *         graphs replayed concurrently) must not share a workspace: one per
+ *         stream is enough, since calls on one stream run one after the
+ *         other.  It must not overlap any other argument.
  */
 tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride,
                                      tfk_bf16* y, int64_t y_row_stride,
                                      const float* weight, const float* shift, const float* scale,
                                      const int32_t* mod_idx, int32_t n_mod,
-                                     int64_t rows, int32_t hidden, float eps, void* stream);
+                                     int64_t rows, int32_t hidden, float eps,
+                                     void* workspace, void* stream);
 
 /*
  * Q/K per-head RMSNorm fused with NeoX rotate-half RoPE (TeleFuser PR #38,
@@ -143,7 +161,7 @@ tfk_status tfk_rmsnorm_adaln_indexed_fixed_valid(const tfk_bf16* x, int64_t x_ro
                                                  const float* scale, const int32_t* mod_idx,
                                                  int32_t n_mod, int64_t valid_rows,
                                                  int64_t padded_rows, int32_t hidden, float eps,
-                                                 void* stream);
+                                                 void* workspace, void* stream);
 
 tfk_status tfk_qk_rmsnorm_rope_neox_fixed_valid(const tfk_bf16* q, const tfk_bf16* k,
                                                 int64_t in_row_stride, tfk_bf16* q_out,

@@ -30,11 +30,11 @@ SIGNATURES = [
     ("tfk_last_error_message", ctypes.c_char_p, []),
     ("tfk_debug_fail_next_launch", ctypes.c_int, [_i32]),
     ("tfk_rmsnorm_adaln_indexed", ctypes.c_int,
-     [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _f32, _vp]),
+     [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _f32, _vp, _vp]),
     ("tfk_qk_rmsnorm_rope_neox", ctypes.c_int,
      [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp]),
     ("tfk_rmsnorm_adaln_indexed_fixed_valid", ctypes.c_int,
-     [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _f32, _vp]),
+     [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _f32, _vp, _vp]),
     ("tfk_qk_rmsnorm_rope_neox_fixed_valid", ctypes.c_int,
      [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _f32, _f32, _vp]),
     ("tfk_qk_rmsnorm_rope_neox_ulysses", ctypes.c_int,
@@ -50,6 +50,10 @@ SIGNATURES = [
 
 _lock = threading.Lock()
 _lib = None
+
+RMSNORM_WORKSPACE_BYTES = 2304  # TFK_RMSNORM_WORKSPACE_BYTES
+_ws_lock = threading.Lock()
+_ws: dict = {}  # (device index, stream handle) -> zeroed int64 tensor of the RMSNorm workspace
 
 
 class TfkError(RuntimeError):
@@ -93,6 +97,36 @@ def _ptr(t: torch.Tensor | None) -> int:
     return 0 if t is None else t.data_ptr()
 
 
+def _workspace(device: torch.device, stream: int, workspace) -> int:
+    """Device address of the RMSNorm workspace for a call on `stream`.
+
+    workspace=None: one zeroed workspace per (device, stream), made on first use
+    (its zero-fill ordered on that stream) and kept; calls on one stream never
+    overlap, and every completed call leaves it zero.  No new one is made while a
+    stream is being captured into a graph (the call then runs without one).
+    workspace=False or 0: none.  A tensor: its own storage (CUDA, at least
+    RMSNORM_WORKSPACE_BYTES bytes, zero before its first use)."""
+    if workspace is None:
+        key = (device.index, stream)
+        ws = _ws.get(key)
+        if ws is None:
+            if torch.cuda.is_current_stream_capturing():
+                return 0
+            with _ws_lock:
+                ws = _ws.get(key)
+                if ws is None:
+                    with torch.cuda.stream(torch.cuda.ExternalStream(stream, device=device)):
+                        ws = torch.zeros(RMSNORM_WORKSPACE_BYTES // 8, dtype=torch.int64, device=device)
+                    _ws[key] = ws
+        return ws.data_ptr()
+    if workspace is False or (isinstance(workspace, int) and workspace == 0):
+        return 0
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or \
+            workspace.numel() * workspace.element_size() < RMSNORM_WORKSPACE_BYTES:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {RMSNORM_WORKSPACE_BYTES} bytes")
+    return workspace.data_ptr()
+
+
 def _rows(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> int:
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -115,8 +149,9 @@ def abi_version() -> int:
 
 def tfk_rmsnorm_adaln_indexed(x: torch.Tensor, weight: torch.Tensor, shift: torch.Tensor,
                               scale: torch.Tensor, mod_idx: torch.Tensor, eps: float = 1e-6,
-                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = RMSNorm(x) * weight * (1 + scale[mod_idx]) + shift[mod_idx]; x, y [rows, hidden] bf16."""
+                              out: torch.Tensor | None = None, stream=None, workspace=None) -> torch.Tensor:
+    """y = RMSNorm(x) * weight * (1 + scale[mod_idx]) + shift[mod_idx]; x, y [rows, hidden] bf16.
+    `workspace`: see _workspace (default: one per stream, managed here)."""
     xs = _rows(x, "x")
     rows, hidden = x.shape
     for t, n in ((weight, "weight"), (shift, "shift"), (scale, "scale")):
@@ -125,9 +160,10 @@ def tfk_rmsnorm_adaln_indexed(x: torch.Tensor, weight: torch.Tensor, shift: torc
     if out is None:
         out = torch.empty((rows, hidden), dtype=torch.bfloat16, device=x.device)
     ys = _rows(out, "out")
+    st = _stream(x, stream)
     _check(load().tfk_rmsnorm_adaln_indexed(_ptr(x), xs, _ptr(out), ys, _ptr(weight), _ptr(shift),
                                             _ptr(scale), _ptr(mod_idx), shift.shape[0] if shift.dim() == 2 else 1,
-                                            rows, hidden, eps, _stream(x, stream)))
+                                            rows, hidden, eps, _workspace(x.device, st, workspace), st))
     return out
 
 
@@ -161,7 +197,7 @@ def tfk_qk_rmsnorm_rope_neox(q: torch.Tensor, k: torch.Tensor, q_weight: torch.T
 def tfk_rmsnorm_adaln_indexed_fixed_valid(x: torch.Tensor, valid_rows: int, weight: torch.Tensor,
                                           shift: torch.Tensor, scale: torch.Tensor, mod_idx: torch.Tensor,
                                           eps: float = 1e-6, out: torch.Tensor | None = None,
-                                          stream=None) -> torch.Tensor:
+                                          stream=None, workspace=None) -> torch.Tensor:
     """Fixed-valid RMSNorm+AdaLN on a padded buffer x [padded_rows, hidden]: rows < valid_rows
     as tfk_rmsnorm_adaln_indexed, the rest of out written +0.0; mod_idx holds valid_rows entries."""
     xs = _rows(x, "x")
@@ -172,9 +208,11 @@ def tfk_rmsnorm_adaln_indexed_fixed_valid(x: torch.Tensor, valid_rows: int, weig
     if out is None:
         out = torch.empty((padded, hidden), dtype=torch.bfloat16, device=x.device)
     ys = _rows(out, "out")
+    st = _stream(x, stream)
     _check(load().tfk_rmsnorm_adaln_indexed_fixed_valid(
         _ptr(x), xs, _ptr(out), ys, _ptr(weight), _ptr(shift), _ptr(scale), _ptr(mod_idx),
-        shift.shape[0] if shift.dim() == 2 else 1, valid_rows, out.shape[0], hidden, eps, _stream(x, stream)))
+        shift.shape[0] if shift.dim() == 2 else 1, valid_rows, out.shape[0], hidden, eps,
+        _workspace(x.device, st, workspace), st))
     return out
 
 

@@ -266,7 +266,7 @@ namespace {
 tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
                       int64_t y_row_stride, const float* weight, const float* shift, const float* scale,
                       const int32_t* mod_idx, int32_t n_mod, int64_t rows, int64_t padded_rows,
-                      int32_t hidden, float eps, void* stream) {
+                      int32_t hidden, float eps, void* workspace, void* stream) {
     if (rows < 0 || padded_rows < rows)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: need 0 <= rows (%lld) <= padded rows (%lld)", op,
                     (long long)rows, (long long)padded_rows);
@@ -294,11 +294,20 @@ tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, t
     if (ranges_overlap(y, ybytes, weight, (int64_t)hidden * 4) || ranges_overlap(y, ybytes, shift, mbytes) ||
         ranges_overlap(y, ybytes, scale, mbytes) || ranges_overlap(y, ybytes, mod_idx, rows * 4))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: y overlaps a parameter buffer", op);
+    if (workspace) {
+        const int64_t wsb = TFK_RMSNORM_WORKSPACE_BYTES;
+        if (!aligned(workspace, 8)) return fail(TFK_ERR_MISALIGNED, "%s: workspace needs 8-byte alignment", op);
+        if (ranges_overlap(workspace, wsb, y, ybytes) ||
+            ranges_overlap(workspace, wsb, x, rows > 0 ? extent_bytes(rows, x_row_stride, hidden, 2) : 0) ||
+            ranges_overlap(workspace, wsb, weight, (int64_t)hidden * 4) || ranges_overlap(workspace, wsb, shift, mbytes) ||
+            ranges_overlap(workspace, wsb, scale, mbytes) || ranges_overlap(workspace, wsb, mod_idx, rows * 4))
+            return fail(TFK_ERR_INVALID_ARGUMENT, "%s: workspace overlaps another argument", op);
+    }
     tfk_status st;
     if (take_injected(op, &st)) return st;
     clear_stale_error();
     tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, padded_rows,
-                     hidden, eps};
+                     hidden, eps, static_cast<unsigned long long*>(workspace)};
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     return finish_launch(op, on_device(stream, [&] { return tfk::launch_rmsnorm_adaln(a, n_mod, s); }));
 }
@@ -381,18 +390,18 @@ extern "C" {
 tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
                                      int64_t y_row_stride, const float* weight, const float* shift,
                                      const float* scale, const int32_t* mod_idx, int32_t n_mod,
-                                     int64_t rows, int32_t hidden, float eps, void* stream) {
+                                     int64_t rows, int32_t hidden, float eps, void* workspace, void* stream) {
     return adaln_impl("tfk_rmsnorm_adaln_indexed", x, x_row_stride, y, y_row_stride, weight, shift, scale,
-                      mod_idx, n_mod, rows, rows, hidden, eps, stream);
+                      mod_idx, n_mod, rows, rows, hidden, eps, workspace, stream);
 }
 
 tfk_status tfk_rmsnorm_adaln_indexed_fixed_valid(const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
                                                  int64_t y_row_stride, const float* weight, const float* shift,
                                                  const float* scale, const int32_t* mod_idx, int32_t n_mod,
                                                  int64_t valid_rows, int64_t padded_rows, int32_t hidden,
-                                                 float eps, void* stream) {
+                                                 float eps, void* workspace, void* stream) {
     return adaln_impl("tfk_rmsnorm_adaln_indexed_fixed_valid", x, x_row_stride, y, y_row_stride, weight, shift,
-                      scale, mod_idx, n_mod, valid_rows, padded_rows, hidden, eps, stream);
+                      scale, mod_idx, n_mod, valid_rows, padded_rows, hidden, eps, workspace, stream);
 }
 
 tfk_status tfk_qk_rmsnorm_rope_neox(const tfk_bf16* q, const tfk_bf16* k, int64_t in_row_stride,

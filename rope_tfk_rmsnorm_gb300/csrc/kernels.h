@@ -29,6 +29,9 @@ struct AdalnArgs {
     int64_t padded_rows;  // rows [rows, padded_rows) of y are written +0.0 (== rows: none)
     int hidden;
     float eps;
+    // Optional (may be null): [0] next row to hand out, [1] CTAs finished;
+    // zero before the launch, left zero by its last CTA.
+    unsigned long long* sched;
 };
 cudaError_t launch_rmsnorm_adaln(const AdalnArgs& a, int n_mod, cudaStream_t stream);
 

@@ -71,9 +71,12 @@ def test_abi_version_and_status_strings(lib):
     assert lib.tfk_status_string(77).decode() == "TFK_ERR_UNKNOWN"
 
 
+WS = 0x70000000
+
+
 def adaln(lib, x=A, xs=512, y=B, ys=512, w=W, sh=S, sc=S + 0x100000, idx=P, n_mod=2, rows=10,
-          hidden=512, eps=1e-6):
-    return lib.tfk_rmsnorm_adaln_indexed(x, xs, y, ys, w, sh, sc, idx, n_mod, rows, hidden, eps, None)
+          hidden=512, eps=1e-6, ws=WS):
+    return lib.tfk_rmsnorm_adaln_indexed(x, xs, y, ys, w, sh, sc, idx, n_mod, rows, hidden, eps, ws, None)
 
 
 def test_adaln_validation(lib):
@@ -96,6 +99,11 @@ def test_adaln_validation(lib):
     assert adaln(lib, y=A + 16) == INVALID and "overlaps x" in msg(lib)     # partial overlap
     assert adaln(lib, y=A, ys=1024, xs=512) == INVALID                      # same base, other stride
     assert adaln(lib, y=W) == INVALID and "parameter" in msg(lib)
+    assert passes_validation(lib, lambda: adaln(lib, ws=0))                  # no workspace: rows split up front
+    assert adaln(lib, ws=WS + 4) == MISALIGNED and "workspace" in msg(lib)
+    assert adaln(lib, ws=B + 64) == INVALID and "workspace overlaps" in msg(lib)   # inside y
+    assert adaln(lib, ws=A + 8) == INVALID and "workspace overlaps" in msg(lib)    # inside x
+    assert adaln(lib, ws=P) == INVALID and "workspace overlaps" in msg(lib)        # on mod_idx
 
 
 def qk(lib, q=A, k=A + 2 * 1024, ist=3 * 1024, qo=B, ko=B + 2 * 1024, ost=3 * 1024, wq=W, wk=W + 64,
@@ -178,7 +186,7 @@ def test_python_binding_rejects_bad_tensors_before_the_abi():
 
 def test_fixed_valid_validation(lib):
     fa = lambda L=10, N=16, x=A, y=B, idx=P: lib.tfk_rmsnorm_adaln_indexed_fixed_valid(
-        x, 512, y, 512, W, S, S + 0x100000, idx, 2, L, N, 512, 1e-6, None)
+        x, 512, y, 512, W, S, S + 0x100000, idx, 2, L, N, 512, 1e-6, WS, None)
     assert passes_validation(lib, fa)
     assert passes_validation(lib, lambda: fa(L=0, x=0, idx=0))              # the whole buffer becomes +0.0
     assert passes_validation(lib, lambda: fa(y=A))                          # in place

@@ -174,6 +174,32 @@ def test_adaln_ragged(cuda, rows, hidden, n_mod, kind):
     check_close(got, ora_adaln(x, w, sh, sc, idx, 1e-6), f"adaln {rows}x{hidden}")
 
 
+@pytest.mark.parametrize("rows,hidden,n_mod", [(30358, 3072, 2), (8192, 3072, 4), (5000, 4352, 3), (3001, 1536, 2),
+                                           (2000, 5120, 2), (600, 2304, 70), (333, 1000, 5)])
+def test_adaln_workspace_and_static_split_give_the_same_bits(cuda, rows, hidden, n_mod):
+    """With a workspace the warp-per-row kernel hands rows out dynamically; without one it
+    splits them up front.  Both give the same bits (a row's arithmetic does not depend on
+    who computes it), and each call leaves the workspace zero for the next.  Also for the
+    fixed-valid variant and for widths the workspace does not change (CTA-per-row)."""
+    rng = np.random.default_rng(rows + hidden)
+    x = to_dev(rand_bits(rng, (rows, hidden)))
+    w, sh, sc = (f32_dev(a) for a in mod_params(rng, n_mod, hidden))
+    idx = i32_dev(rng.integers(0, n_mod, rows).astype(np.int32))
+    ws = torch.zeros(tfk.RMSNORM_WORKSPACE_BYTES // 8, dtype=torch.int64, device="cuda")
+    plain = tfk.tfk_rmsnorm_adaln_indexed(x, w, sh, sc, idx, 1e-6, workspace=False)
+    first = tfk.tfk_rmsnorm_adaln_indexed(x, w, sh, sc, idx, 1e-6, workspace=ws)
+    second = tfk.tfk_rmsnorm_adaln_indexed(x, w, sh, sc, idx, 1e-6, workspace=ws)
+    L = rows - rows // 7
+    fv_plain = tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(x, L, w, sh, sc, idx[:L], 1e-6, workspace=False)
+    fv_ws = tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(x, L, w, sh, sc, idx[:L], 1e-6, workspace=ws)
+    torch.cuda.synchronize()
+    bits = lambda t: t.view(torch.int16)
+    assert torch.equal(bits(plain), bits(first)) and torch.equal(bits(plain), bits(second))
+    assert torch.equal(bits(fv_plain), bits(fv_ws))
+    assert torch.equal(bits(fv_ws[:L]), bits(plain[:L])) and int((bits(fv_ws[L:]) != 0).sum()) == 0
+    assert int(ws.abs().sum()) == 0, "the workspace is not left zero"
+
+
 def test_adaln_strided_and_in_place(cuda):
     rng = np.random.default_rng(1)
     rows, hidden = 211, 3072
