@@ -111,6 +111,40 @@ tfk_status tfk_rmsnorm_adaln_indexed(const tfk_bf16* x, int64_t x_row_stride,
                                      void* workspace, void* stream);
 
 /*
+ * RMSNorm + indexed AdaLN exactly as tfk_rmsnorm_adaln_indexed, for callers
+ * that cannot allocate device memory.  The pages have no counterpart: this
+ * is an interface of this library.
+ *
+ * Some callers have no way to hand the library a workspace: code that runs
+ * where device allocation is not allowed or not wanted (cudaMalloc
+ * synchronises the device and cannot be recorded into a stream capture, and a
+ * real-time loop or a plugin running inside another runtime's stream often may
+ * not call it), or that does not own an allocator at all.  This entry point
+ * takes the same arguments as tfk_rmsnorm_adaln_indexed without the workspace
+ * and allocates nothing: the row counters the warp-per-row kernel uses live in
+ * a 4096-byte array of the library (a file-scope device variable; each GPU
+ * that loads the library holds it until the process exits), of which a call
+ * needs TFK_RMSNORM_WORKSPACE_BYTES whatever its sizes, so no size can exceed
+ * it; sizes are limited as for tfk_rmsnorm_adaln_indexed.  Each call clears the
+ * counters on its stream (cudaMemsetAsync) before its kernel.
+ *
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and keeps it; make that
+ *   first call before capturing a stream into a graph.
+ * - Every call shares the one array, which keeps what the last call left in
+ *   it: calls that may run at the same time on one GPU (on other streams)
+ *   race on it and may compute wrong rows.  Issue them on one stream, or use
+ *   tfk_rmsnorm_adaln_indexed with a workspace per stream.
+ * Errors as for tfk_rmsnorm_adaln_indexed.
+ */
+tfk_status tfk_rmsnorm_adaln_indexed_noalloc(const tfk_bf16* x, int64_t x_row_stride,
+                                             tfk_bf16* y, int64_t y_row_stride,
+                                             const float* weight, const float* shift,
+                                             const float* scale, const int32_t* mod_idx,
+                                             int32_t n_mod, int64_t rows, int32_t hidden,
+                                             float eps, void* stream);
+
+/*
  * Q/K per-head RMSNorm fused with NeoX rotate-half RoPE (TeleFuser PR #38,
  * section 2, the Q/K norm + RoPE fusion; TeleFuser PR #23, section Changes
  * Made, the Q/K normalization with NeoX RoPE kernel).  For q (with q_weight)

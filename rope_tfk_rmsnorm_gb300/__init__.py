@@ -31,6 +31,8 @@ SIGNATURES = [
     ("tfk_debug_fail_next_launch", ctypes.c_int, [_i32]),
     ("tfk_rmsnorm_adaln_indexed", ctypes.c_int,
      [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _f32, _vp, _vp]),
+    ("tfk_rmsnorm_adaln_indexed_noalloc", ctypes.c_int,
+     [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _f32, _vp]),
     ("tfk_qk_rmsnorm_rope_neox", ctypes.c_int,
      [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp]),
     ("tfk_rmsnorm_adaln_indexed_fixed_valid", ctypes.c_int,
@@ -164,6 +166,24 @@ def tfk_rmsnorm_adaln_indexed(x: torch.Tensor, weight: torch.Tensor, shift: torc
     _check(load().tfk_rmsnorm_adaln_indexed(_ptr(x), xs, _ptr(out), ys, _ptr(weight), _ptr(shift),
                                             _ptr(scale), _ptr(mod_idx), shift.shape[0] if shift.dim() == 2 else 1,
                                             rows, hidden, eps, _workspace(x.device, st, workspace), st))
+    return out
+
+
+def tfk_rmsnorm_adaln_indexed_noalloc(x: torch.Tensor, weight: torch.Tensor, shift: torch.Tensor,
+                                      scale: torch.Tensor, mod_idx: torch.Tensor, out: torch.Tensor,
+                                      eps: float = 1e-6, stream=None) -> torch.Tensor:
+    """tfk_rmsnorm_adaln_indexed into a caller-given `out`, with no workspace and no allocation
+    (the row counters live in an array of the library; calls that overlap on one GPU race)."""
+    xs = _rows(x, "x")
+    rows, hidden = x.shape
+    for t, n in ((weight, "weight"), (shift, "shift"), (scale, "scale")):
+        _param(t, n)
+    _param(mod_idx, "mod_idx", torch.int32)
+    ys = _rows(out, "out")
+    _check(load().tfk_rmsnorm_adaln_indexed_noalloc(_ptr(x), xs, _ptr(out), ys, _ptr(weight), _ptr(shift),
+                                                    _ptr(scale), _ptr(mod_idx),
+                                                    shift.shape[0] if shift.dim() == 2 else 1, rows, hidden, eps,
+                                                    _stream(x, stream)))
     return out
 
 

@@ -263,10 +263,13 @@ tfk_status tfk_debug_fail_next_launch(int32_t cuda_error) {
 namespace {
 
 // rows are computed from x; rows [rows, padded_rows) of y are written +0.0.
-tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
-                      int64_t y_row_stride, const float* weight, const float* shift, const float* scale,
-                      const int32_t* mod_idx, int32_t n_mod, int64_t rows, int64_t padded_rows,
-                      int32_t hidden, float eps, void* workspace, void* stream) {
+// The argument checks of the RMSNorm+AdaLN entry points; *empty is set when
+// the call has nothing to compute (no rows at all).
+tfk_status adaln_check(const char* op, const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
+                       int64_t y_row_stride, const float* weight, const float* shift, const float* scale,
+                       const int32_t* mod_idx, int32_t n_mod, int64_t rows, int64_t padded_rows,
+                       int32_t hidden, float eps, void* workspace, bool* empty) {
+    *empty = false;
     if (rows < 0 || padded_rows < rows)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: need 0 <= rows (%lld) <= padded rows (%lld)", op,
                     (long long)rows, (long long)padded_rows);
@@ -278,7 +281,10 @@ tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, t
     if (x_row_stride < hidden || y_row_stride < hidden)
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: row strides (%lld, %lld) must be >= hidden %d", op,
                     (long long)x_row_stride, (long long)y_row_stride, hidden);
-    if (padded_rows == 0) return ok();
+    if (padded_rows == 0) {
+        *empty = true;
+        return ok();
+    }
     if (!y || (rows > 0 && (!x || !weight || !shift || !scale || !mod_idx)))
         return fail(TFK_ERR_INVALID_ARGUMENT, "%s: null pointer", op);
     if (x_row_stride % 8 || y_row_stride % 8)
@@ -303,6 +309,17 @@ tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, t
             ranges_overlap(workspace, wsb, scale, mbytes) || ranges_overlap(workspace, wsb, mod_idx, rows * 4))
             return fail(TFK_ERR_INVALID_ARGUMENT, "%s: workspace overlaps another argument", op);
     }
+    return ok();
+}
+
+tfk_status adaln_impl(const char* op, const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
+                      int64_t y_row_stride, const float* weight, const float* shift, const float* scale,
+                      const int32_t* mod_idx, int32_t n_mod, int64_t rows, int64_t padded_rows,
+                      int32_t hidden, float eps, void* workspace, void* stream) {
+    bool empty = false;
+    const tfk_status chk = adaln_check(op, x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, n_mod,
+                                       rows, padded_rows, hidden, eps, workspace, &empty);
+    if (chk != TFK_OK || empty) return chk;
     tfk_status st;
     if (take_injected(op, &st)) return st;
     clear_stale_error();
@@ -548,3 +565,76 @@ tfk_status tfk_zero_tail_merge(const tfk_bf16* compact, tfk_bf16* padded, int64_
 }
 
 }  // extern "C"
+
+// ---- RMSNorm+AdaLN without any allocation by the caller ----------------------
+//
+// tfk_rmsnorm_adaln_indexed_noalloc runs the same computation as
+// tfk_rmsnorm_adaln_indexed, with the scratch the warp-per-row kernel uses
+// (its row counters) in an array of this library instead of a workspace from
+// the caller.  The array is a file-scope device variable: every GPU that loads
+// the library holds it until the process exits.  In host code its name only
+// stands for it; its device address comes from cudaGetSymbolAddress, taken
+// once per device with that device current and cached.  Every call uses the
+// same array, so calls that may run at the same time on one GPU race on it.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4096;  // the array; a call needs TFK_RMSNORM_WORKSPACE_BYTES of it
+static_assert(TFK_RMSNORM_WORKSPACE_BYTES <= kNoAllocScratchBytes,
+              "the no-allocation scratch array is smaller than the RMSNorm workspace");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[tfk::kMaxDevicesForScratch];
+
+// Device address of g_noalloc_scratch on the current device (set up on the
+// first call for that device).
+cudaError_t noalloc_scratch(void** addr) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= tfk::kMaxDevicesForScratch) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" tfk_status tfk_rmsnorm_adaln_indexed_noalloc(const tfk_bf16* x, int64_t x_row_stride, tfk_bf16* y,
+                                                        int64_t y_row_stride, const float* weight,
+                                                        const float* shift, const float* scale,
+                                                        const int32_t* mod_idx, int32_t n_mod, int64_t rows,
+                                                        int32_t hidden, float eps, void* stream) {
+    static const char* op = "tfk_rmsnorm_adaln_indexed_noalloc";
+    bool empty = false;
+    const tfk_status chk = adaln_check(op, x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, n_mod,
+                                       rows, rows, hidden, eps, nullptr, &empty);
+    if (chk != TFK_OK || empty) return chk;
+    // The scratch a call needs does not grow with its sizes, so no size can
+    // exceed the array; kept as a check in case the workspace ever grows.
+    if ((size_t)TFK_RMSNORM_WORKSPACE_BYTES > kNoAllocScratchBytes)
+        return fail(TFK_ERR_UNSUPPORTED, "%s: needs %d bytes of scratch, more than the %zu-byte array", op,
+                    TFK_RMSNORM_WORKSPACE_BYTES, kNoAllocScratchBytes);
+    tfk_status st;
+    if (take_injected(op, &st)) return st;
+    clear_stale_error();
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return finish_launch(op, on_device(stream, [&]() -> cudaError_t {
+        void* scratch = nullptr;
+        cudaError_t err = noalloc_scratch(&scratch);
+        if (err != cudaSuccess) return err;
+        // The counters must start at zero: clear them on the call's stream
+        // (a completed call also leaves them zero).
+        if ((err = cudaMemsetAsync(scratch, 0, TFK_RMSNORM_WORKSPACE_BYTES, s)) != cudaSuccess) return err;
+        tfk::AdalnArgs a{x, x_row_stride, y, y_row_stride, weight, shift, scale, mod_idx, rows, rows,
+                         hidden, eps, static_cast<unsigned long long*>(scratch)};
+        return tfk::launch_rmsnorm_adaln(a, n_mod, s);
+    }));
+}

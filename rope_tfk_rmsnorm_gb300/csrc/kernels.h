@@ -8,6 +8,9 @@
 
 namespace tfk {
 
+// Devices a process may use with this library's per-device caches.
+constexpr int kMaxDevicesForScratch = 64;
+
 // Attributes of the current device, read once per device and cached.
 struct DeviceInfo {
     int sm_count;
