@@ -683,7 +683,9 @@ def graph_ms(unit, reps: int) -> float:
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
+    # Captured on the stream of the warm-up call, so that the binding's workspace
+    # for that stream (RMSNorm+AdaLN's row counters) exists and the graph uses it.
+    with torch.cuda.graph(g, stream=side):
         for _ in range(reps):
             unit.launch()
     g.replay()

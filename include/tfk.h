@@ -96,7 +96,8 @@ tfk_status tfk_debug_fail_next_launch(int32_t cuda_error);
  *         that keep the rows' modulation in shared memory hand rows to warps
  *         as they become free (a row counter in the workspace) instead of
  *         splitting the rows evenly up front, which keeps every SM busy to
- *         the end; the output bits are the same either way.  It must be zero
+ *         the end, in calls large enough for that to pay (x at least 336 KiB
+ *         per SM); the output bits are the same either way.  It must be zero
  *         before its first use; every call that completes leaves it zero.
  *         Calls that may run at the same time on the GPU (other streams,
  *         graphs replayed concurrently) must not share a workspace: one per

@@ -439,10 +439,10 @@ rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots, const int n_mod) {
     // its group with one atomic on the group's counter.  Measured (fraction of
     // the copy bandwidth, event-timed) against rows split up front: 30,358 x
     // 3072 0.79 -> 0.85, 75,600 x 3072 0.88 -> 0.95, 30,000 x 4352 0.81 ->
-    // 0.88, 8,192 x 3072 equal.  One counter for all SMs queued the claims at
-    // 75,600 x 3072 (0.59); two counters 0.89, four and eight 0.94-0.95.
-    // Claiming one row ahead, or several rows per claim in shrinking chunks,
-    // measured 1-6 points lower.
+    // 0.88 (smaller calls get no counters: kHandOutMinBytesPerSm).  One
+    // counter for all SMs queued the claims at 75,600 x 3072 (0.59); two
+    // counters 0.89, four and eight 0.94-0.95.  Claiming one row ahead, or
+    // several rows per claim in shrinking chunks, measured 1-6 points lower.
     const bool dynamic = a.sched != nullptr && slots >= n_mod;
     const int groups = gridDim.x < (unsigned)kSchedGroups ? (int)gridDim.x : kSchedGroups;
     const int grp = (int)(blockIdx.x % (unsigned)groups);
@@ -491,6 +491,13 @@ rmsnorm_adaln_warp_kernel(const AdalnArgs a, const int slots, const int n_mod) {
 
         // The claimed modulation rows, staged as one flat loop over
         // (slot, vector) so that all their loads are in flight together.
+        // Building the table costs 1.2-3 us per launch (measured by leaving it
+        // out: 8,192 x 3072 26.0 -> 24.3 us, 30,000 x 6144 120 -> 117 us).
+        // Measured equal or slower: shift and scale copied into the table
+        // with cp.async and combined in place (+4.5 us at 8,192 x 3072), w
+        // read once per half-vector for all slots, the warp's first row issued
+        // or prefetched into L2 before the table, and a first row per warp
+        // assigned without a claim.
         const int items = n_claimed * nvec;
 #pragma unroll 2
         for (int it = tid; it < items; it += nt) {
@@ -683,11 +690,24 @@ bool use_warp_kernel(int hidden) {
     return v == 3 || (v == 4 && !exact);
 }
 
+// Rows are handed out (when a workspace is given) only if each SM's share of
+// x is at least this many bytes; below it every warp has only a few rows, the
+// claims cost more than the balance brings, and the rows are split up front.
+// Measured (fraction of the copy bandwidth, back to back, static / handed
+// out): hidden 3072 at 4,000 rows 0.57 / 0.52, 8,192 0.71 / 0.68, 11,000
+// 0.76 / 0.77, 14,600 0.79 / 0.82; hidden 1536 at 14,600 rows 0.74 / 0.70,
+// 19,456 0.77 / 0.76, 29,000 0.80 / 0.82; hidden 6144 at 4,300 rows 0.64 /
+// 0.66.  The crossing sits near 400 KB per SM for 1536 and 3072 and lower
+// for 6144.
+constexpr int64_t kHandOutMinBytesPerSm = 336 * 1024;
+
 template <int VPL, bool kExact>
-cudaError_t launch_warp(const AdalnArgs& a, int n_mod, cudaStream_t stream) {
+cudaError_t launch_warp(const AdalnArgs& a_in, int n_mod, cudaStream_t stream) {
     DeviceInfo di;
     cudaError_t err = device_info(&di);
     if (err != cudaSuccess) return err;
+    AdalnArgs a = a_in;
+    if (a.rows * a.hidden * 2 < kHandOutMinBytesPerSm * di.sm_count) a.sched = nullptr;
     const int64_t slot_bytes = (int64_t)a.hidden * 8;
     int64_t slots = ((int64_t)di.max_smem_per_block_optin - 2048) / slot_bytes;
     if (slots > n_mod) slots = n_mod;

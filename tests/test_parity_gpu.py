@@ -174,13 +174,16 @@ def test_adaln_ragged(cuda, rows, hidden, n_mod, kind):
     check_close(got, ora_adaln(x, w, sh, sc, idx, 1e-6), f"adaln {rows}x{hidden}")
 
 
-@pytest.mark.parametrize("rows,hidden,n_mod", [(30358, 3072, 2), (8192, 3072, 4), (5000, 4352, 3), (3001, 1536, 2),
-                                           (2000, 5120, 2), (600, 2304, 70), (333, 1000, 5)])
+@pytest.mark.parametrize("rows,hidden,n_mod", [(30358, 3072, 2), (20001, 4352, 3), (40000, 1536, 2), (12000, 6144, 2),
+                                           (10007, 5632, 4), (8192, 3072, 4), (3001, 1536, 2), (2000, 5120, 2),
+                                           (20000, 2304, 70), (333, 1000, 5)])
 def test_adaln_workspace_and_static_split_give_the_same_bits(cuda, rows, hidden, n_mod):
-    """With a workspace the warp-per-row kernel hands rows out dynamically; without one it
-    splits them up front.  Both give the same bits (a row's arithmetic does not depend on
-    who computes it), and each call leaves the workspace zero for the next.  Also for the
-    fixed-valid variant and for widths the workspace does not change (CTA-per-row)."""
+    """With a workspace the warp-per-row kernel hands rows out dynamically (calls of at least
+    336 KiB of x per SM: the first five cases on a 152-SM GPU); without one it splits them up
+    front.  Both give the same bits (a row's arithmetic does not depend on who computes it),
+    and each call leaves the workspace zero for the next.  Also for the fixed-valid variant,
+    for calls below that size, for more modulation rows than shared-memory slots (2304 x 70,
+    several passes) and for widths the workspace does not change (CTA-per-row)."""
     rng = np.random.default_rng(rows + hidden)
     x = to_dev(rand_bits(rng, (rows, hidden)))
     w, sh, sc = (f32_dev(a) for a in mod_params(rng, n_mod, hidden))
