@@ -202,3 +202,57 @@ def test_back_to_back_dependent_launches_keep_stream_order(cuda):
 def synth_f32(bits: np.ndarray) -> np.ndarray:
     """Raw bf16 bits -> float32 values."""
     return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def test_graph_capture_of_the_fixed_valid_ulysses_and_handed_out_calls(cuda):
+    """The entry points the chain tests do not capture: both fixed-valid kernels, Q/K
+    written into the Ulysses send layout, and RMSNorm+AdaLN with rows handed out through
+    a caller's workspace (18,000 x 3072: above the size from which rows are handed out),
+    captured into a CUDA graph and replayed twice; each replay gives the eager bits and
+    leaves the workspace zero."""
+    wl, p, d = _problem(rows=18000, name="graph2")
+    T, hd, H, D = wl.rows, wl.hidden, wl.n_heads, wl.head_dim
+    L = T - 1234
+    ws = torch.zeros(tfk.RMSNORM_WORKSPACE_BYTES // 8, dtype=torch.int64, device=cuda)
+
+    def launch(out):
+        tfk.tfk_rmsnorm_adaln_indexed(d["x"], p["w"], p["shift"], p["scale"], d["idx"], wl.eps, out=out["y"],
+                                      workspace=ws)
+        tfk.tfk_rmsnorm_adaln_indexed_fixed_valid(d["x"], L, p["w"], p["shift"], p["scale"], d["idx"][:L], wl.eps,
+                                                  out=out["fy"], workspace=ws)
+        tfk.tfk_qk_rmsnorm_rope_neox_fixed_valid(d["q"], d["k"], L, p["w_q"], p["w_k"], d["pos"][:L], H, D,
+                                                 wl.theta, wl.eps, q_out=out["fq"], k_out=out["fk"])
+        tfk.tfk_qk_rmsnorm_rope_neox_ulysses(d["q"], d["k"], p["w_q"], p["w_k"], d["pos"], H, D, 4, wl.theta,
+                                             wl.eps, q_send=out["sq"], k_send=out["sk"])
+
+    def outputs():
+        send = (4, T, H // 4, D)
+        return {"y": torch.empty_like(d["x"]), "fy": torch.empty_like(d["x"]),
+                "fq": torch.empty_like(d["q"]), "fk": torch.empty_like(d["k"]),
+                "sq": torch.empty(send, dtype=torch.bfloat16, device=cuda),
+                "sk": torch.empty(send, dtype=torch.bfloat16, device=cuda)}
+
+    ref = outputs()
+    launch(ref)
+    torch.cuda.synchronize()
+    want = {k: to_host(v) for k, v in ref.items()}
+    assert int(ws.abs().sum()) == 0
+
+    got = outputs()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        launch(outputs())                          # warm the library's per-device caches outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch(got)
+    for _ in range(2):
+        for t in got.values():
+            t.fill_(-1.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for k, v in got.items():
+            assert np.array_equal(to_host(v), want[k]), k
+        assert int(ws.abs().sum()) == 0, "a replay left the workspace non-zero"
