@@ -49,15 +49,22 @@ namespace {
 // persistent run of ~166 tokens per CTA (whose static split leaves some SMs
 // idle at the end) and 85% with a 102-register cap; 4-token chunks measured
 // 1-4% above 8 on all four workload shapes, 8 above 16 and 24.
+// Four heads per lane group, every group full and no token streams (the
+// head counts of every workload here: 24, 32, 40) take 2-token chunks and a
+// 96-register cap (four CTAs per SM) instead: measured (fraction of the
+// copy bandwidth, event-timed, against 4-token chunks and 136 registers)
+// 8,192 x 24 heads 0.766 -> 0.788, 30,358 x 24 0.949 -> 0.960, 75,600 x 40
+// 1.023 -> 1.029, 56,320 x 32 1.004 -> 1.011; 1-token chunks 0.69-0.89, 3
+// tokens between the two.  With masked groups (25 heads: 0.87 -> 0.80) or
+// token streams (6 heads: 0.73 -> 0.69) the same change loses, so those keep
+// 4-token chunks and 136 registers.
 constexpr int kMaxThreads = 160;
-#ifndef TFK_A2_MIN_BLOCKS
-#define TFK_A2_MIN_BLOCKS 3
-#endif
-#ifndef TFK_A2_ROWS_PER_CTA
-#define TFK_A2_ROWS_PER_CTA 4  // 0: one persistent run of tokens per resident CTA
-#endif
-constexpr int kMinBlocks = TFK_A2_MIN_BLOCKS;
-constexpr int64_t kRowsPerCta = TFK_A2_ROWS_PER_CTA;
+template <int HPT, bool kMasked, bool kStreams>
+constexpr bool kDense = HPT == 4 && !kMasked && !kStreams;
+template <int HPT, bool kMasked, bool kStreams>
+constexpr int kMinBlocks = kDense<HPT, kMasked, kStreams> ? 4 : 3;
+template <int HPT, bool kMasked, bool kStreams>
+constexpr int64_t kRowsPerCta = kDense<HPT, kMasked, kStreams> ? 2 : 4;
 
 __device__ __forceinline__ void rope_cos_sin(int32_t pos, uint64_t turn_fraction, float& c, float& s) {
     const uint64_t a = (uint64_t)(int64_t)pos * turn_fraction;        // mod 2^64 = mod one turn
@@ -101,7 +108,7 @@ struct Layout {
 };
 
 template <int HPT, bool kMasked, bool kStreams>
-__global__ void __launch_bounds__(kMaxThreads, kMinBlocks) qk_rope_kernel(const QkRopeArgs a, const Layout lay,
+__global__ void __launch_bounds__(kMaxThreads, (kMinBlocks<HPT, kMasked, kStreams>)) qk_rope_kernel(const QkRopeArgs a, const Layout lay,
                                                               const int token_chunks, const int stages,
                                                               const __grid_constant__ RopeTable tab) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -361,8 +368,8 @@ cudaError_t launch_h(const QkRopeArgs& a, const Layout& lay, cudaStream_t stream
     // token runs: enough CTAs for every SM, and no more runs than rows to work on
     int64_t want = ((int64_t)per_sm * di.sm_count + lay.head_chunks - 1) / lay.head_chunks;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
-    if constexpr (kRowsPerCta > 0) {  // fixed-size chunks instead of one persistent run per CTA
-        const int64_t per = (kRowsPerCta > 0 ? kRowsPerCta : 1) * lay.streams;  // rows per stream stay kRowsPerCta
+    {  // fixed-size chunks instead of one persistent run per CTA
+        const int64_t per = kRowsPerCta<HPT, kMasked, kStreams> * lay.streams;  // rows per stream stay the chunk
         const int64_t chunks = (work + per - 1) / per;
         if (chunks > want) want = chunks;
     }
