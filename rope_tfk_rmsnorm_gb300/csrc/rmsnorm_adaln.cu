@@ -40,17 +40,20 @@ namespace {
 constexpr int kMaxThreads = 512;
 constexpr int kMaxThreadsV1 = 384;
 // Rows per CTA: one persistent run per resident CTA, unless such a run would
-// exceed kChunkMinRun rows; then chunks of kRowsPerCta rows that the hardware
-// block scheduler balances over the SMs.  Measured on the GB300: chunks of 24
-// gain 1.5-2% at 56,320-75,600 rows (runs of 93-166 rows), while at 30,358
-// rows of 3072 (runs of 40) the persistent split is 4% faster.
-#ifndef TFK_A1_ROWS_PER_CTA
-#define TFK_A1_ROWS_PER_CTA 24
-#endif
+// exceed kChunkMinRun rows; then chunks of kRowsPerCta rows (kRowsPerCtaWide
+// for rows of 16 KB and more) that the hardware block scheduler balances over
+// the SMs.  Measured on the GB300: chunks of 24 gain 1.5-2% at 56,320-75,600
+// rows (runs of 93-166 rows), while at 30,358 rows of 3072 (runs of 40) the
+// persistent split is 4% faster.  Chunks of 16 rather than 24 (fraction of
+// the copy bandwidth, event-timed): 75,600 x 5120 0.962 -> 0.974, 56,320 x
+// 4096 0.922 -> 0.929, but 20,000 x 8192 0.758 -> 0.734 (there each chunk
+// also reloads 96 KB of modulation), so wide rows keep 24; 12 and 32 rows
+// measured no better than these.
 #ifndef TFK_A1_CHUNK_MIN_RUN
 #define TFK_A1_CHUNK_MIN_RUN 64
 #endif
-constexpr int64_t kRowsPerCta = TFK_A1_ROWS_PER_CTA;
+constexpr int64_t kRowsPerCta = 16;
+constexpr int64_t kRowsPerCtaWide = 24;
 template <int V, bool kExact>
 constexpr bool kSortRows = V == 2 || (V == 4 && kExact);
 constexpr int kSortRun = 64;  // at most 256: row positions are stored as bytes
@@ -650,8 +653,9 @@ cudaError_t launch_v(const AdalnArgs& a, int threads, cudaStream_t stream) {
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     int64_t grid = (int64_t)per_sm * di.sm_count;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
-    if constexpr (kRowsPerCta > 0) {  // fixed-size chunks instead of long persistent runs
-        const int64_t chunks = (work + kRowsPerCta - 1) / (kRowsPerCta > 0 ? kRowsPerCta : 1);
+    {  // fixed-size chunks instead of long persistent runs
+        const int64_t per = row_bytes >= 16384 ? kRowsPerCtaWide : kRowsPerCta;
+        const int64_t chunks = (work + per - 1) / per;
         if (chunks > grid && work >= kChunkMinRun * grid) grid = chunks;
     }
     if (grid > (1 << 24)) grid = 1 << 24;  // the row split covers any grid; keeps rows * blockIdx in range
@@ -775,7 +779,7 @@ cudaError_t launch_pair(const AdalnArgs& a, int threads, cudaStream_t stream) {
     int64_t pairs = (int64_t)per_sm * di.sm_count / 2;
     if (pairs < 1) pairs = 1;
     const int64_t work = a.rows > a.padded_rows - a.rows ? a.rows : a.padded_rows - a.rows;
-    const int64_t chunks = (work + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t chunks = (work + kRowsPerCtaWide - 1) / kRowsPerCtaWide;
     if (chunks > pairs && work >= kChunkMinRun * pairs) pairs = chunks;
     if (pairs > (1 << 23)) pairs = 1 << 23;
     if (pairs > work) pairs = work;

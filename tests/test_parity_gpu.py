@@ -526,11 +526,11 @@ def _full_chain(wl):
 
 @pytest.mark.parametrize("rows,hidden", [(120000, 512), (50000, 3072), (20000, 16384), (12000, 20480)])
 def test_adaln_chunked_schedule_sampled(cuda, rows, hidden):
-    """One, two and eight vectors per thread at row counts where the RMSNorm
-    kernel hands out 24-row chunks instead of one persistent run per CTA (more
-    than 64 rows per resident CTA): rows at chunk edges, the first and last
-    rows and a seeded sample are recomputed by the oracle; the modulation row
-    is drawn per token from three."""
+    """Row counts where the CTA-per-row RMSNorm kernel hands out chunks (16 rows,
+    24 for rows of 16 KB and more) instead of one persistent run per CTA (more than
+    64 rows per resident CTA), the pair of CTAs per row at 20480, and the warp-per-row
+    kernel at 3072: rows at chunk edges, the first and last rows and a seeded sample
+    are recomputed by the oracle; the modulation row is drawn per token from three."""
     wl = synth.custom(f"chunked{hidden}", rows, hidden, 8, 64, 64, n_mod=3)
     rng = np.random.default_rng(rows + hidden)
     w, sh, sc = mod_params(rng, 3, hidden)
@@ -539,7 +539,7 @@ def test_adaln_chunked_schedule_sampled(cuda, rows, hidden):
     y = tfk.tfk_rmsnorm_adaln_indexed(dev["x"], f32_dev(w), f32_dev(sh), f32_dev(sc), i32_dev(idx), 1e-6)
     torch.cuda.synchronize()
     del dev
-    edges = np.arange(0, rows, 24)
+    edges = np.arange(0, rows, 16 if hidden * 2 < 16384 else 24)
     sample = np.unique(np.r_[edges[::97], edges[::89] - 1, synth.sample_rows(wl, 160)].clip(0, rows - 1))
     got = to_host(y[torch.from_numpy(sample).cuda()])
     del y

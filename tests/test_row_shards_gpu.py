@@ -6,9 +6,10 @@ sequence parallelism of the MiniMax H3 integration (TeleFuser PR #23,
 Changes Made) shards the token sequence exactly this way before its
 all-to-all.
 
-The shards are of unequal size and their edges fall off the 4- and 24-row
-chunk grids of the Q/K and RMSNorm schedules, so each shard gets its own grid,
-chunking and (for RMSNorm) row order; one shard has only 7 rows."""
+The shards are of unequal size and their inner edges (all but the end of
+the one 7-row shard) are odd, so they fall off the 2-, 4-, 16- and 24-row
+chunk grids of the Q/K and RMSNorm schedules and each shard gets its own
+grid, chunking and (for RMSNorm) row order."""
 import numpy as np
 import pytest
 import torch
@@ -22,10 +23,10 @@ pytestmark = pytest.mark.gpu
 
 def _cuts(T: int, n: int) -> list:
     if n == 2:
-        return [0, T // 3 + 1, T]
+        return [0, (T // 3) | 1, T]
     rng = np.random.default_rng(n)
     inner = set(int(c) for c in rng.choice(np.arange(1, T - 8), n - 2, replace=False))
-    inner = {c + 1 if c % 4 == 0 else c for c in inner}   # never on a 4- or 24-row chunk edge
+    inner = {c + 1 if c % 2 == 0 else c for c in inner}   # odd: never on a chunk edge
     c = max(inner)
     inner.add(c + 7)                                       # a shard of 7 rows
     return [0, *sorted(inner), T]
