@@ -85,8 +85,22 @@ def _adaln_warp_cases(n):
     return out
 
 
+def _adaln_handout_cases(n):
+    """Warp-per-row widths at 60-140 MB of x, above the size from which rows are handed
+    out to warps through a workspace, with up to 8 modulation rows (all staged at once)."""
+    whole = [768 * k for k in range(2, 9)]
+    ragged = [h for h in range(4104, 6144, 8) if h % 1024]
+    out = []
+    for i in range(n):
+        hidden = int(_RNG.choice(whole if i % 2 == 0 else ragged))
+        rows = int(_RNG.integers(60_000_000, 140_000_000) // (2 * hidden))
+        out.append((rows, hidden, int(_RNG.integers(1, 9)), int(_RNG.integers(0, 2 ** 31))))
+    return out
+
+
 ADALN = _adaln_cases(40)
 ADALN_WARP = _adaln_warp_cases(10)
+ADALN_HANDOUT = _adaln_handout_cases(6)
 QK = _qk_cases(40)
 SWIGLU = _swiglu_cases(20)
 ULYSSES = _ulysses_cases(16)
@@ -112,6 +126,28 @@ def test_adaln_warp_kernel_random_shapes(cuda, rows, hidden, n_mod, seed):
     idx = rng.integers(0, n_mod, rows).astype(np.int32)
     check_close(gpu_adaln(x, w, sh, sc, idx, 1e-6), ora_adaln(x, w, sh, sc, idx, 1e-6),
                 f"a1 {rows}x{hidden}")
+
+
+@pytest.mark.parametrize("rows,hidden,n_mod,seed", ADALN_HANDOUT,
+                         ids=[f"{r}x{h}m{m}" for r, h, m, _ in ADALN_HANDOUT])
+def test_adaln_rows_handed_out_random_shapes(cuda, rows, hidden, n_mod, seed):
+    """Rows handed out through a workspace give the bits of the split up front on every
+    element, leave the workspace zero, and agree with the oracle on sampled rows."""
+    rng = np.random.default_rng(seed)
+    xh = rand_bits(rng, (rows, hidden), 2.0)
+    x = to_dev(xh)
+    w, sh, sc = mod_params(rng, n_mod, hidden)
+    idx = rng.integers(0, n_mod, rows).astype(np.int32)
+    args = (x, f32_dev(w), f32_dev(sh), f32_dev(sc), i32_dev(idx), 1e-6)
+    ws = torch.zeros(tfk.RMSNORM_WORKSPACE_BYTES // 8, dtype=torch.int64, device="cuda")
+    handed = tfk.tfk_rmsnorm_adaln_indexed(*args, workspace=ws)
+    split = tfk.tfk_rmsnorm_adaln_indexed(*args, workspace=False)
+    torch.cuda.synchronize()
+    assert torch.equal(handed.view(torch.int16), split.view(torch.int16))
+    assert int(ws.abs().sum()) == 0
+    sample = np.unique(np.r_[0, rows - 1, rng.integers(0, rows, 254)])
+    got = handed[torch.from_numpy(sample).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    check_close(got, ora_adaln(xh[sample], w, sh, sc, idx[sample], 1e-6), f"a1 handed out {rows}x{hidden}")
 
 
 @pytest.mark.parametrize("rows,H,D,seed", QK, ids=[f"{r}x{h}x{d}" for r, h, d, _ in QK])
