@@ -106,6 +106,25 @@ def test_adaln_validation(lib):
     assert adaln(lib, ws=P) == INVALID and "workspace overlaps" in msg(lib)        # on mod_idx
 
 
+def adaln_noalloc(lib, x=A, xs=512, y=B, ys=512, w=W, sh=S, sc=S + 0x100000, idx=P, n_mod=2, rows=10,
+                  hidden=512, eps=1e-6):
+    return lib.tfk_rmsnorm_adaln_indexed_noalloc(x, xs, y, ys, w, sh, sc, idx, n_mod, rows, hidden, eps, None)
+
+
+def test_adaln_noalloc_validation(lib):
+    """The allocation-free entry point checks its arguments as tfk_rmsnorm_adaln_indexed
+    does, under its own name, before it touches its scratch array or the GPU."""
+    assert passes_validation(lib, lambda: adaln_noalloc(lib))
+    assert passes_validation(lib, lambda: adaln_noalloc(lib, y=A))          # in place
+    assert adaln_noalloc(lib, rows=0, x=0, y=0, w=0, sh=0, sc=0, idx=0) == OK
+    assert adaln_noalloc(lib, x=0) == INVALID and "tfk_rmsnorm_adaln_indexed_noalloc" in msg(lib)
+    assert adaln_noalloc(lib, n_mod=0) == INVALID
+    assert adaln_noalloc(lib, hidden=32776, xs=32776, ys=32776) == UNSUPPORTED
+    assert adaln_noalloc(lib, xs=516) == MISALIGNED
+    assert adaln_noalloc(lib, y=A + 16) == INVALID and "overlaps x" in msg(lib)
+    assert adaln_noalloc(lib, eps=float("nan")) == INVALID
+
+
 def qk(lib, q=A, k=A + 2 * 1024, ist=3 * 1024, qo=B, ko=B + 2 * 1024, ost=3 * 1024, wq=W, wk=W + 64,
        pos=P, rows=10, H=8, D=128, theta=10000.0, eps=1e-6):
     return lib.tfk_qk_rmsnorm_rope_neox(q, k, ist, qo, ko, ost, wq, wk, pos, rows, H, D, theta, eps, None)
